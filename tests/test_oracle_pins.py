@@ -1,0 +1,476 @@
+"""Pins for the CPU oracle: facts that the pages and mathematics fix.
+
+None of these tests re-types an oracle formula. Each compares the oracle with
+something independent of it: the H4 matrix as printed on the page, NumPy's
+Kronecker product, orthogonality and symmetry, exact rational arithmetic,
+closed forms for one-hot rows, brute-force integer loops, and error bounds.
+The last group plants plausible mistakes in the oracle and checks that some
+pin fails for each of them.
+"""
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import convrot_oracle as orc
+from int8_hadamard_rotated_gb300 import workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+GROUPS = (1, 4, 16, 64, 256, 1024)
+
+
+def printed_h4():
+    rows = []
+    with open(os.path.join(GOLDEN, "h4.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append([int(v) for v in line.split()])
+    return np.array(rows, dtype=np.float64) / 2.0
+
+
+def kron_power(H, G):
+    R = np.ones((1, 1))
+    while R.shape[0] < G:
+        R = np.kron(R, H)
+    return R
+
+
+# --------------------------------------------------------------------------
+# R_G ("INT8 Convrot Safetensors" -- How INT8 convrot works)
+# --------------------------------------------------------------------------
+
+def check_h4(mod=orc):
+    np.testing.assert_array_equal(mod.H4, printed_h4())
+
+
+def check_R_kron(mod=orc):
+    H = printed_h4()
+    for G in (4, 16, 64, 256):
+        R = mod.hadamard_matrix(G)
+        np.testing.assert_array_equal(R, kron_power(H, G))
+        if G > 4:
+            # the factors are identical, so either nesting gives R_G
+            np.testing.assert_array_equal(R, np.kron(H, kron_power(H, G // 4)))
+
+
+def check_R_algebra(mod=orc):
+    for G in GROUPS:
+        R = mod.hadamard_matrix(G)
+        eye = np.eye(G)
+        np.testing.assert_allclose(R @ R.T, eye, atol=1e-12)   # orthogonal
+        np.testing.assert_array_equal(R, R.T)                  # symmetric
+        np.testing.assert_allclose(R @ R, eye, atol=1e-12)     # hence an involution
+        np.testing.assert_allclose(R.sum(axis=1), np.ones(G), atol=1e-12)  # regular
+        np.testing.assert_array_equal(np.abs(R), np.full((G, G), 1.0 / np.sqrt(G)))
+
+
+def test_h4_is_the_printed_matrix():
+    check_h4()
+
+
+def test_R_is_the_kronecker_power():
+    check_R_kron()
+
+
+def test_R_orthogonal_symmetric_regular():
+    check_R_algebra()
+
+
+def test_group_rule():
+    for G in GROUPS:
+        assert orc.is_valid_group(G, 3 * G)
+    for G in (2, 3, 8, 12, 32, 128, 512, 0, -4):
+        assert not orc.is_valid_group(G, 4096)
+    assert not orc.is_valid_group(256, 1000)
+    with pytest.raises(ValueError):
+        orc.rotate(np.zeros((2, 96), np.float32), 64)
+
+
+# --------------------------------------------------------------------------
+# rotation
+# --------------------------------------------------------------------------
+
+def _exact_fp32_round(fr: Fraction) -> np.float32:
+    """Round an exact rational to the nearest fp32 (ties to even), by search."""
+    x = np.float32(float(fr))           # within a few ulp of the answer
+    cands = [x]
+    for _ in range(3):
+        cands.append(np.nextafter(cands[-1], np.float32(np.inf)))
+    y = x
+    for _ in range(3):
+        y = np.nextafter(y, np.float32(-np.inf))
+        cands.append(y)
+    best = min(cands, key=lambda c: (abs(Fraction(float(c)) - fr),
+                                     int(np.array(c).view(np.int32)) & 1))
+    return np.float32(best)
+
+
+def check_rotate_exact(mod=orc):
+    """Brute force: each output is the exact dot product with the group's
+    R column (exact rationals), rounded once to fp32."""
+    rng = workloads.rng_for(11)
+    H = printed_h4()
+    for G, K in ((4, 12), (16, 32), (64, 64)):
+        X = workloads.activations(rng, 3, K, outlier_frac=0.1, outlier_mult=30.0)
+        Rf = [[Fraction(v) for v in row] for row in kron_power(H, G)]
+        got = mod.rotate(X, G)
+        for r in range(3):
+            for c in range(K):
+                g0 = (c // G) * G
+                acc = Fraction(0)
+                for i in range(G):
+                    acc += Fraction(float(X[r, g0 + i])) * Rf[i][c - g0]
+                assert got[r, c] == _exact_fp32_round(acc), (G, r, c)
+
+
+def test_rotate_is_the_correctly_rounded_product():
+    check_rotate_exact()
+
+
+def test_rotation_identity_fp64():
+    """X R (W R)^T = X W^T (How INT8 convrot works), fp64 on small inputs."""
+    rng = workloads.rng_for(12)
+    for G in (4, 16, 64, 256):
+        K = 2 * G
+        X = rng.standard_normal((5, K))
+        W = rng.standard_normal((7, K))
+        R = np.kron(np.eye(K // G), orc.hadamard_matrix(G))
+        lhs = (X @ R) @ (W @ R).T
+        np.testing.assert_allclose(lhs, X @ W.T, rtol=1e-12, atol=1e-12)
+
+
+def test_rotation_keeps_row_norms_and_groups():
+    rng = workloads.rng_for(13)
+    X = workloads.activations(rng, 8, 1024, outlier_frac=0.02, outlier_mult=40.0)
+    for G in GROUPS:
+        Y = orc.rotate(X, G).astype(np.float64)
+        x64 = X.astype(np.float64)
+        for g in range(1024 // G):
+            sl = slice(g * G, (g + 1) * G)
+            np.testing.assert_allclose(np.linalg.norm(Y[:, sl], axis=1),
+                                       np.linalg.norm(x64[:, sl], axis=1), rtol=1e-6)
+    np.testing.assert_array_equal(orc.rotate(X, 1), X)   # G = 1 is the identity
+
+
+def test_rotation_of_group_constant_rows():
+    """Rows of R sum to 1, so a row constant on each group is unchanged."""
+    for G in (4, 16, 64, 256, 1024):
+        X = np.repeat(np.array([[1.5, -2.0, 0.25]], np.float32), G, axis=1)
+        np.testing.assert_array_equal(orc.rotate(X, G), X)
+
+
+def test_one_hot_closed_form():
+    """x = c e_j spreads to +-c/sqrt(G) over its group: |Q| = 127 there,
+    zero elsewhere, s = (|c|/sqrt G)/127 (the outlier-spreading purpose)."""
+    K = 2048
+    for G in (4, 16, 64, 256, 1024):
+        for j, c in ((0, 3.0), (G + 5, -40.0), (K - 1, 1000.0)):
+            X = np.zeros((1, K), np.float32)
+            X[0, j] = c
+            Q, s = orc.pack(X, G)
+            g0 = (j // G) * G
+            mag = np.float32(abs(c) / np.sqrt(G))
+            assert s[0] == np.float32(mag / np.float32(127))
+            R = orc.hadamard_matrix(G)
+            expect = np.zeros(K, np.int8)
+            expect[g0:g0 + G] = (np.sign(c) * np.sign(R[j - g0])).astype(np.int8) * 127
+            np.testing.assert_array_equal(Q[0], expect)
+
+
+# --------------------------------------------------------------------------
+# quantizer (Runtime activation quantization / Weight quantization)
+# --------------------------------------------------------------------------
+
+def check_round_half_even(mod=orc):
+    # row max 254 -> s = 2 exactly; x/s lands exactly on k + 1/2
+    X = np.array([[254, 1, 3, 5, -1, -3, 7, 0]], np.float32)
+    Q, s = mod.quantize_rows(X)
+    assert s[0] == np.float32(2.0)
+    np.testing.assert_array_equal(Q[0], np.array([127, 0, 2, 2, 0, -2, 4, 0], np.int8))
+
+
+def test_round_half_to_even():
+    check_round_half_even()
+
+
+def check_quantizer_invariants(mod=orc):
+    rng = workloads.rng_for(14)
+    X = workloads.activations(rng, 64, 512, outlier_frac=0.01, outlier_mult=50.0)
+    for G in (1, 4, 64, 256):
+        Xr = mod.rotate(X, G)
+        Q, s = mod.quantize_rows(Xr)
+        assert Q.dtype == np.int8 and s.dtype == np.float32
+        assert Q.min() >= -127 and Q.max() <= 127
+        np.testing.assert_array_equal(np.abs(Q).max(axis=1), 127)
+        amax = np.abs(Xr).max(axis=1).astype(np.float64)
+        np.testing.assert_allclose(s.astype(np.float64), amax / 127.0, rtol=2**-23)
+        err = np.abs(Xr.astype(np.float64) - Q.astype(np.float64) * s[:, None])
+        assert np.all(err <= s[:, None] * (0.5 + 1e-5))
+        # odd symmetry and monotonicity of the quantizer within each row
+        Qn, sn = mod.quantize_rows(-Xr)
+        np.testing.assert_array_equal(Qn, -Q)
+        np.testing.assert_array_equal(sn, s)
+        order = np.argsort(Xr, axis=1, kind="stable")
+        assert np.all(np.diff(np.take_along_axis(Q.astype(np.int32), order, axis=1), axis=1) >= 0)
+
+
+def test_quantizer_invariants():
+    check_quantizer_invariants()
+
+
+def test_zero_rows():
+    X = np.zeros((3, 256), np.float32)
+    X[1, 7] = 2.0
+    Q, s = orc.pack(X, 256)
+    assert s[0] == 0 and s[2] == 0 and s[1] > 0
+    assert not Q[0].any() and not Q[2].any()
+
+
+def test_g1_is_plain_absmax_quantization():
+    """G = 1: the rotation is the identity and the pack is textbook per-row
+    absmax quantization; compare with a direct Fraction-based evaluation of
+    round(x / s) where s and x/s are fp32 results."""
+    rng = workloads.rng_for(15)
+    X = workloads.activations(rng, 4, 32, outlier_frac=0.1, outlier_mult=20.0)
+    Q, s = orc.pack(X, 1)
+    for r in range(4):
+        a = max(abs(Fraction(float(v))) for v in X[r])
+        s_r = _exact_fp32_round(a / 127)
+        assert s[r] == s_r
+        for i in range(32):
+            qf = _exact_fp32_round(Fraction(float(X[r, i])) / Fraction(float(s_r)))
+            qi = int(np.rint(np.float64(qf)))
+            assert Q[r, i] == max(-127, min(127, qi))
+
+
+# --------------------------------------------------------------------------
+# integer GEMM and reconstruction
+# --------------------------------------------------------------------------
+
+def check_gemm_bruteforce(mod=orc):
+    rng = workloads.rng_for(16)
+    Qx = workloads.random_codes(rng, 5, 48)
+    Qw = workloads.random_codes(rng, 7, 48)
+    A = mod.gemm_s32(Qx, Qw)
+    assert A.dtype == np.int32 and A.shape == (5, 7)
+    for r in range(5):
+        for o in range(7):
+            assert A[r, o] == sum(int(Qx[r, i]) * int(Qw[o, i]) for i in range(48))
+
+
+def test_gemm_bruteforce():
+    check_gemm_bruteforce()
+
+
+def test_gemm_extremes():
+    K = 133144  # largest K whose worst case fits int32: 133144 * 127^2 < 2^31
+    Qx = np.full((2, K), 127, np.int8)
+    Qw = np.full((2, K), 127, np.int8)
+    Qw[1] = -127
+    A = orc.gemm_s32(Qx, Qw)
+    assert A[0, 0] == K * 127 * 127 and A[0, 1] == -K * 127 * 127
+    with pytest.raises(OverflowError):
+        orc.gemm_s32(np.zeros((1, K + 1), np.int8), np.zeros((1, K + 1), np.int8))
+
+
+def check_reconstruct_exact(mod=orc):
+    A = np.array([[3, -8], [0, 1 << 20]], np.int32)
+    s_x = np.array([0.5, 2.0], np.float32)
+    s_w = np.array([0.25, 4.0], np.float32)
+    b = np.array([1.0, -0.5], np.float32)
+    Y = mod.reconstruct(A, s_x, s_w, b)
+    np.testing.assert_array_equal(Y, np.array([[1.375, -16.5], [1.0, 8.0 * (1 << 20) - 0.5]], np.float32))
+    np.testing.assert_array_equal(mod.reconstruct(A, s_x), np.array([[1.5, -4.0], [0.0, 2.0 * (1 << 20)]], np.float32))
+    np.testing.assert_array_equal(mod.reconstruct(A, s_x, None, b), np.array([[2.5, -4.5], [1.0, 2.0 * (1 << 20) - 0.5]], np.float32))
+
+
+def test_reconstruct_exact_cases():
+    check_reconstruct_exact()
+
+
+def test_reconstruct_rounds_int32_once():
+    """|A| above 2^24 is itself rounded when converted to fp32."""
+    A = np.array([[(1 << 24) + 1]], np.int32)
+    Y = orc.reconstruct(A, np.array([1.0], np.float32), np.array([1.0], np.float32), np.array([0.0], np.float32))
+    assert Y[0, 0] == np.float32(1 << 24)
+
+
+def check_linear_error_bound(mod=orc):
+    """Y differs from X W^T + b by at most the quantization error bound
+    sum_i |x_rot_i| s_w/2 + |q_w,i s_w| s_x/2 (plus fp32 rounding)."""
+    case = workloads.make_case(workloads.get("tiny"))
+    X, W, b = case.X, case.Ws[0], case.bs[0]
+    G = 256
+    Qw, s_w = mod.prepare_weight(W, G)
+    Y = mod.linear(X, Qw, s_w, b, G)
+    ref = X.astype(np.float64) @ W.astype(np.float64).T + b
+    Xr = mod.rotate(X, G).astype(np.float64)
+    _, s_x = mod.pack(X, G)
+    wq = Qw.astype(np.float64) * s_w[:, None]
+    bound = (np.abs(Xr) @ np.ones_like(wq.T)) * (s_w[None, :] / 2) \
+        + (np.ones_like(Xr) @ np.abs(wq).T) * (s_x[:, None] / 2)
+    err = np.abs(Y - ref)
+    assert np.all(err <= bound * 1.001 + 1e-5), float(np.max(err / bound))
+    # and the approximation is useful: error well below the output scale
+    assert np.max(err) < 0.05 * np.max(np.abs(ref))
+
+
+def test_linear_within_quantization_error():
+    check_linear_error_bound()
+
+
+def test_rotation_spreads_outliers():
+    """With a channel outlier the rotated quantization error is smaller than
+    the unrotated one (the purpose stated in How INT8 convrot works)."""
+    rng = workloads.rng_for(17)
+    X = workloads.activations(rng, 64, 1024, outlier_kind="channel",
+                              outlier_frac=0.005, outlier_mult=30.0)
+    def rel_err(G):
+        Q, s = orc.pack(X, G)
+        Xr = orc.rotate(X, G).astype(np.float64)
+        return np.linalg.norm(Xr - Q * s[:, None].astype(np.float64)) / np.linalg.norm(Xr)
+    assert rel_err(256) < 0.5 * rel_err(1)
+
+
+def test_gelu_reference_points():
+    y = np.array([0.0, 1.0, -1.0, 3.0], np.float32)
+    # Phi(1) = 0.8413447460685429..., Phi(3) = 0.9986501019683699
+    expect = np.array([0.0, 0.8413447460685429, -0.15865525393145707, 3 * 0.9986501019683699])
+    np.testing.assert_allclose(orc.gelu(y), expect.astype(np.float32), rtol=1e-7)
+
+
+# --------------------------------------------------------------------------
+# planted mistakes: each must trip at least one pin
+# --------------------------------------------------------------------------
+
+class _Mutant:
+    """A copy of the oracle namespace with one function replaced."""
+
+    def __init__(self, **over):
+        for k in dir(orc):
+            if not k.startswith("__"):
+                setattr(self, k, getattr(orc, k))
+        for k, v in over.items():
+            setattr(self, k, v)
+        # rebind helpers that call each other through the module
+        me = self
+
+        def pack(X, G):
+            return me.quantize_rows(me.rotate(X, G))
+
+        def prepare_weight(W, G):
+            return me.quantize_rows(me.rotate(W, G))
+
+        def linear(X, Qw, s_w, bias, G):
+            Qx, s_x = me.pack(X, G)
+            return me.reconstruct(me.gemm_s32(Qx, Qw), s_x, s_w, bias)
+
+        for name, fn in (("pack", pack), ("prepare_weight", prepare_weight), ("linear", linear)):
+            if name not in over:
+                setattr(self, name, fn)
+
+
+def _fails(mod, checks):
+    for chk in checks:
+        try:
+            chk(mod)
+        except AssertionError:
+            return True
+    return False
+
+
+ALL_CHECKS = (check_h4, check_R_kron, check_R_algebra, check_rotate_exact,
+              check_round_half_even, check_quantizer_invariants,
+              check_gemm_bruteforce, check_reconstruct_exact, check_linear_error_bound)
+
+
+def _bad_h4():
+    H = orc.H4.copy()
+    H[2, 3] = -H[2, 3]
+    return H
+
+
+def _rotate_wrong_axis(X, G):
+    M, K = X.shape
+    R = orc.hadamard_matrix(G)
+    x = X.astype(np.float64).reshape(M, K // G, G)
+    # groups taken with stride K/G instead of contiguous
+    x = X.astype(np.float64).reshape(M, G, K // G).transpose(0, 2, 1)
+    y = np.einsum("rgi,ij->rgj", x, R)
+    return y.transpose(0, 2, 1).reshape(M, K).astype(np.float32)
+
+
+def _rotate_unnormalised(X, G):
+    return (orc.rotate(X, G).astype(np.float64) * np.sqrt(G)).astype(np.float32)
+
+
+def _quant_half_away(Xrot):
+    Xrot = np.asarray(Xrot, np.float32)
+    s = (np.abs(Xrot).max(axis=1) / np.float32(127)).astype(np.float32)
+    q = Xrot / s[:, None]
+    q = np.sign(q) * np.floor(np.abs(q) + 0.5)
+    return np.clip(q, -127, 127).astype(np.int8), s
+
+
+def _quant_scale_255(Xrot):
+    Xrot = np.asarray(Xrot, np.float32)
+    s = (np.abs(Xrot).max(axis=1) / np.float32(255)).astype(np.float32)
+    q = np.rint(Xrot / s[:, None])
+    return np.clip(q, -128, 127).astype(np.int8), s
+
+
+def _gemm_transposed(Qx, Qw):
+    return orc.gemm_s32(Qx, Qw[::-1])
+
+
+def _gemm_offby(Qx, Qw):
+    return orc.gemm_s32(Qx[:, 1:], Qw[:, :-1])
+
+
+def _recon_no_sw(A, s_x, s_w=None, bias=None):
+    return orc.reconstruct(A, s_x, None, bias)
+
+
+def _recon_minus_bias(A, s_x, s_w=None, bias=None):
+    Y = orc.reconstruct(A, s_x, s_w, None)
+    return Y if bias is None else (Y - np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+
+
+@pytest.mark.parametrize("mutant", [
+    dict(H4=_bad_h4()),
+    dict(rotate=_rotate_wrong_axis),
+    dict(rotate=_rotate_unnormalised),
+    dict(quantize_rows=_quant_half_away),
+    dict(quantize_rows=_quant_scale_255),
+    dict(gemm_s32=_gemm_transposed),
+    dict(gemm_s32=_gemm_offby),
+    dict(reconstruct=_recon_no_sw),
+    dict(reconstruct=_recon_minus_bias),
+], ids=["h4-sign", "rotate-strided-groups", "rotate-unnormalised", "round-half-away",
+        "scale-255", "gemm-transposed", "gemm-shifted", "recon-no-sw", "recon-minus-bias"])
+def test_planted_mistakes_are_caught(mutant):
+    if "H4" in mutant:
+        # H4 feeds hadamard_matrix through the module global
+        bad = mutant["H4"]
+
+        def hm(G, _bad=bad):
+            n = 0
+            while 4**n < G:
+                n += 1
+            R = np.ones((G, G))
+            idx = np.arange(G)
+            for k in range(n):
+                d = (idx // 4**k) % 4
+                R *= _bad[d[:, None], d[None, :]]
+            return R
+        mutant = dict(mutant, hadamard_matrix=hm)
+    assert _fails(_Mutant(**mutant), ALL_CHECKS)
+
+
+def test_oracle_package_exports():
+    for name in ("H4", "hadamard_matrix", "rotate", "quantize_rows", "pack",
+                 "prepare_weight", "gemm_s32", "reconstruct", "linear", "gelu"):
+        assert hasattr(oracle, name)
