@@ -1,0 +1,220 @@
+/*
+ * convrot.h -- C ABI of libconvrot.so, the INT8 "convrot" linear layer on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (stable-diffusion.cpp documentation, page
+ * "INT8 Convrot Safetensors"):
+ *   - "How INT8 convrot works": R_G = H4^{(x)n}, the normalized Kronecker
+ *     power of the regular Hadamard matrix H4 for a group size G = 4^n,
+ *     applied to every contiguous group of G input features: X_rot = X R,
+ *     W_rot = W R.
+ *   - "Weight quantization": s_w[o] = max_i |W_rot[o,i]| / 127,
+ *     Q_w[o,i] = clamp(round(W_rot[o,i] / s_w[o]), -127, 127).
+ *   - "Runtime activation quantization": s_x[r] = max_i |X_rot[r,i]| / 127
+ *     over the whole rotated row, Q_x by the same rule, the int32 product
+ *     A[r,o] = sum_i Q_x[r,i] Q_w[o,i], and Y ~= A s_x[r] s_w[o] + b[o];
+ *     linears sharing an input and a group size reuse one packed activation.
+ *   - page "ggml operator extensions", section "sd.cpp integration": the
+ *     output is float(A) * s_x * s_w + bias evaluated in that order, with the
+ *     weight scale and the bias optional.
+ *
+ * Conventions for every entry point
+ *   - Matrices are dense and row-major: X is [M,K] (K contiguous), W and the
+ *     weight codes are [N,K], Y and A are [M,N].
+ *   - Every array pointer is a DEVICE pointer on the current CUDA device,
+ *     owned by the caller; the library keeps no pointer after a call returns
+ *     and allocates no device memory. Arrays must start on a 16-byte boundary.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream). Work is enqueued asynchronously on it; the return value only
+ *     reports argument checks and launch errors. Faults found later by a
+ *     kernel (a bounded device-side wait that gave up) are reported by
+ *     convrot_device_status().
+ *   - Rounding: "round" is round-half-to-even; the two divisions of the
+ *     quantizer are IEEE fp32 divisions; an all-zero row has scale 0 and
+ *     codes 0.
+ *   - The tensor cores of sm_103a have no 8-bit integer MMA, so the GEMM runs
+ *     on the fp16 tensor-core path: int8 codes are exact in IEEE binary16, each
+ *     K-chunk of at most 1024 products is summed exactly in fp32 (its partial
+ *     sums stay below 2^24) and the chunk sums are added in int32. The int32
+ *     result is therefore bit-exact. Weight codes are also kept as binary16
+ *     ("Q_w16", written by convrot_prepare_weight) so the GEMM reads them
+ *     directly.
+ */
+#ifndef CONVROT_H
+#define CONVROT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. Every entry point returns one of these (as int). */
+typedef enum convrot_status {
+  CONVROT_OK = 0,
+  CONVROT_ERR_ARG = 1,         /* NULL where an array is required, a size < 0,
+                                  an unknown dtype, n_weights outside [1,8] */
+  CONVROT_ERR_GROUP = 2,       /* G is not 4^n with 1 <= G <= 1024, or K % G != 0
+                                  ("Checkpoint format": a power of four that
+                                  divides the input feature dimension) */
+  CONVROT_ERR_ALIGN = 3,       /* an array not 16-byte aligned, or K % 16 != 0 */
+  CONVROT_ERR_OVERFLOW = 4,    /* K * 127^2 > INT32_MAX (K > 133144): the int32
+                                  accumulation could overflow */
+  CONVROT_ERR_ALIAS = 5,       /* an output array overlaps an input or another
+                                  output */
+  CONVROT_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than the size query */
+  CONVROT_ERR_UNSUPPORTED = 7, /* a shape beyond this build's limits (pack rows
+                                  longer than CONVROT_PACK_MAX_K) */
+  CONVROT_ERR_TIMEOUT = 8,     /* a kernel's bounded wait gave up (from
+                                  convrot_device_status) */
+  CONVROT_ERR_CUDA = 9,        /* a CUDA runtime call failed or a launch error;
+                                  convrot_last_cuda_error() gives the code */
+  CONVROT_ERR_DEVICE = 10      /* the current device is not an sm_103 GPU */
+} convrot_status;
+
+/* Element type of the floating-point activation input X. */
+typedef enum convrot_dtype {
+  CONVROT_F32 = 0, /* IEEE binary32 */
+  CONVROT_F16 = 1  /* IEEE binary16 (converted exactly to fp32 on load) */
+} convrot_dtype;
+
+/* Longest activation row (K) the pack kernel holds on chip. */
+#define CONVROT_PACK_MAX_K 32768
+/* Largest K whose worst-case int32 accumulation fits: 133144 * 127^2 < 2^31. */
+#define CONVROT_MAX_K 133144
+/* Most linears one convrot_linear call may share a packed input across. */
+#define CONVROT_MAX_LINEARS 8
+
+/* Library version, major*10000 + minor*100 + patch. */
+int convrot_version(void);
+
+/* Static text for a convrot_status value. */
+const char* convrot_strerror(int status);
+
+/* The cudaError_t of the most recent CONVROT_ERR_CUDA on this host thread. */
+int convrot_last_cuda_error(void);
+
+/*
+ * convrot_prepare_weight -- offline weight path ("Weight quantization").
+ *   W      [N,K] fp32 weights (input).
+ *   G      group size, 4^n in [1,1024], dividing K.
+ *   Q_w    [N,K] int8 codes (output).
+ *   s_w    [N] fp32 per-output-row scales (output).
+ *   Q_w16  [N,K] the same codes as binary16 (output, may be NULL; required by
+ *          convrot_linear and used by int8_linear when given).
+ * Same rotation and quantizer as convrot_pack_activations, applied to W.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_prepare_weight(const float* W, int64_t N, int64_t K, int G,
+                           int8_t* Q_w, float* s_w, uint16_t* Q_w16,
+                           void* stream);
+
+/*
+ * convrot_pack_activations -- runtime activation quantization.
+ *   X       [M,K] activations, fp32 or fp16 per x_dtype (input).
+ *   Q_x     [M,K] int8 codes (output).
+ *   s_x     [M] fp32 row scales (output).
+ * One pass over X: group-wise rotation, row absmax over the whole rotated
+ * row, quantization. M = 0 is a no-op. K <= CONVROT_PACK_MAX_K.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_pack_activations(const void* X, int x_dtype, int64_t M, int64_t K,
+                             int G, int8_t* Q_x, float* s_x, void* stream);
+
+/*
+ * int8_linear_workspace_size -- device bytes int8_linear needs: room to widen
+ * Q_x (and Q_w when Q_w16 is not given) to binary16 codes.
+ */
+size_t int8_linear_workspace_size(int64_t M, int64_t N, int64_t K,
+                                  int have_q_w16);
+
+/*
+ * int8_linear -- Y = float(Q_x Q_w^T) * s_x[r] * s_w[o] + bias[o].
+ *   Q_x    [M,K] int8, s_x [M] fp32 (e.g. from convrot_pack_activations).
+ *   Q_w    [N,K] int8 codes; may be NULL when Q_w16 is given.
+ *   Q_w16  [N,K] binary16 codes, or NULL (then Q_w is widened in workspace).
+ *   s_w    [N] fp32 or NULL (taken as 1).   bias [N] fp32 or NULL (none).
+ *   Y      [M,N] fp32 (output).
+ *   workspace / workspace_bytes: device scratch, at least
+ *          int8_linear_workspace_size(M, N, K, Q_w16 != NULL) bytes.
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS, ERR_WORKSPACE, ERR_CUDA.
+ */
+int int8_linear(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
+                const int8_t* Q_w, const uint16_t* Q_w16, const float* s_w,
+                const float* bias, int64_t N, float* Y,
+                void* workspace, size_t workspace_bytes, void* stream);
+
+/* One linear of a convrot_linear call. */
+typedef struct convrot_weight {
+  const uint16_t* q16; /* [N,K] binary16 weight codes (convrot_prepare_weight) */
+  const float* scale;  /* [N] s_w, or NULL (taken as 1) */
+  const float* bias;   /* [N], or NULL (no bias) */
+  int64_t N;           /* output features */
+  float* Y;            /* [M,N] fp32 output */
+} convrot_weight;
+
+/* Device bytes convrot_linear needs for the shared packed activation. */
+size_t convrot_linear_workspace_size(int64_t M, int64_t K);
+
+/*
+ * convrot_linear -- n_weights linears sharing one input and group size:
+ * X is packed once (rotation, row scales, codes) into the workspace, then one
+ * grouped GEMM computes every Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j.
+ *   X         [M,K] fp32/fp16 activations.
+ *   weights   host array of n_weights descriptors (1 <= n_weights <= 8); all
+ *             Y_j must be distinct and must not overlap X or any weight.
+ *   workspace at least convrot_linear_workspace_size(M, K) bytes.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS,
+ *         ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
+                   const convrot_weight* weights, int n_weights,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * int8_gemm_s32 -- the raw int32 product A = Q_x Q_w^T (no scales), through
+ * the same tensor-core GEMM as int8_linear. For exactness checks.
+ *   Arguments as int8_linear; A [M,N] int32 (output).
+ * Errors: as int8_linear.
+ */
+int int8_gemm_s32(const int8_t* Q_x, int64_t M, int64_t K,
+                  const int8_t* Q_w, const uint16_t* Q_w16, int64_t N,
+                  int32_t* A, void* workspace, size_t workspace_bytes,
+                  void* stream);
+
+/*
+ * convrot_pack_activations_f16 -- the pack of convrot_pack_activations, with
+ * the codes written as binary16 integers: the packed activation in the form
+ * the tensor-core GEMM reads. One packed activation can feed any number of
+ * convrot_linear_packed calls ("Runtime activation quantization": linears
+ * sharing an input and group size reuse the packed tensor).
+ *   Q_x16  [M,K] binary16 codes (output).   s_x [M] fp32 (output).
+ * Errors: as convrot_pack_activations.
+ */
+int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t K,
+                                 int G, uint16_t* Q_x16, float* s_x, void* stream);
+
+/*
+ * convrot_linear_packed -- the grouped GEMM of convrot_linear on an activation
+ * packed by convrot_pack_activations_f16: every
+ * Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j. Needs no workspace.
+ *   Q_x16 [M,K] binary16 codes, s_x [M] fp32; weights as convrot_linear.
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS, ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
+                          const convrot_weight* weights, int n_weights, void* stream);
+
+/*
+ * convrot_device_status -- synchronizes `stream`, then returns and clears the
+ * device's sticky error word: CONVROT_OK, or CONVROT_ERR_TIMEOUT when a
+ * kernel's bounded wait on a TMA or tensor-core completion barrier gave up
+ * (the kernel then skipped its remaining work and released its resources).
+ */
+int convrot_device_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVROT_H */

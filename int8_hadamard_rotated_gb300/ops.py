@@ -1,0 +1,273 @@
+"""Thin Python binding of libconvrot.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls and does no
+arithmetic of its own: it checks dtypes/devices, allocates outputs and
+workspace with PyTorch when the caller does not pass them, and hands raw
+device pointers plus the current CUDA stream to the library. All compute runs
+in the library's sm_103a kernels; if the library is missing this module
+raises, there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import List, Optional, Sequence, Tuple
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libconvrot.so")
+
+# status codes (include/convrot.h)
+OK = 0
+ERR_ARG = 1
+ERR_GROUP = 2
+ERR_ALIGN = 3
+ERR_OVERFLOW = 4
+ERR_ALIAS = 5
+ERR_WORKSPACE = 6
+ERR_UNSUPPORTED = 7
+ERR_TIMEOUT = 8
+ERR_CUDA = 9
+ERR_DEVICE = 10
+
+F32 = 0
+F16 = 1
+MAX_LINEARS = 8
+PACK_MAX_K = 32768
+MAX_K = 133144
+
+
+class ConvrotError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _lib_or_none()
+        msg = lib.convrot_strerror(status).decode() if lib else str(status)
+        if status == ERR_CUDA and lib:
+            msg += f" (cudaError {lib.convrot_last_cuda_error()})"
+        super().__init__(f"{where}: {msg} [status {status}]")
+        self.status = status
+
+
+class convrot_weight(ctypes.Structure):
+    _fields_ = [("q16", ctypes.c_void_p), ("scale", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p), ("N", ctypes.c_int64),
+                ("Y", ctypes.c_void_p)]
+
+
+_LIB = None
+
+_VP, _I64, _I, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+SIGNATURES = {
+    "convrot_version": (_I, []),
+    "convrot_strerror": (ctypes.c_char_p, [_I]),
+    "convrot_last_cuda_error": (_I, []),
+    "convrot_prepare_weight": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP, _VP]),
+    "convrot_pack_activations": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
+    "int8_linear_workspace_size": (_SZ, [_I64, _I64, _I64, _I]),
+    "int8_linear": (_I, [_VP, _VP, _I64, _I64, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "convrot_linear_workspace_size": (_SZ, [_I64, _I64]),
+    "convrot_linear": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
+    "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
+    "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
+    "convrot_device_status": (_I, [_VP]),
+}
+
+
+def _lib_or_none():
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    """Load libconvrot.so (once). Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"{LIB_PATH} is missing: build it with "
+                "`python -m int8_hadamard_rotated_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise ConvrotError(status, where)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else stream
+
+
+def _need(t: torch.Tensor, dtype, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _xdtype(X: torch.Tensor) -> int:
+    if X.dtype == torch.float32:
+        return F32
+    if X.dtype == torch.float16:
+        return F16
+    raise ValueError("X must be float32 or float16")
+
+
+# ---------------------------------------------------------------------------
+
+def convrot_pack_activations(X: torch.Tensor, G: int, Q_x: Optional[torch.Tensor] = None,
+                             s_x: Optional[torch.Tensor] = None, stream=None
+                             ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Rotate and quantize the rows of X [M,K] -> (Q_x int8 [M,K], s_x f32 [M])."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    if Q_x is None:
+        Q_x = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _need(Q_x, torch.int8, "Q_x")
+    _need(s_x, torch.float32, "s_x")
+    _check(lib().convrot_pack_activations(_ptr(X), xd, M, K, G, _ptr(Q_x), _ptr(s_x), _stream(stream)),
+           "convrot_pack_activations")
+    return Q_x, s_x
+
+
+def convrot_prepare_weight(W: torch.Tensor, G: int, with_f16: bool = True, stream=None):
+    """Offline weight path: W [N,K] f32 -> (Q_w int8, s_w f32, Q_w16 fp16 codes or None)."""
+    _need(W, torch.float32, "W")
+    N, K = W.shape
+    Q_w = torch.empty((N, K), dtype=torch.int8, device=W.device)
+    s_w = torch.empty((N,), dtype=torch.float32, device=W.device)
+    Q_w16 = torch.empty((N, K), dtype=torch.float16, device=W.device) if with_f16 else None
+    _check(lib().convrot_prepare_weight(_ptr(W), N, K, G, _ptr(Q_w), _ptr(s_w), _ptr(Q_w16), _stream(stream)),
+           "convrot_prepare_weight")
+    return Q_w, s_w, Q_w16
+
+
+def int8_linear_workspace_size(M: int, N: int, K: int, have_q_w16: bool) -> int:
+    return int(lib().int8_linear_workspace_size(M, N, K, 1 if have_q_w16 else 0))
+
+
+def convrot_linear_workspace_size(M: int, K: int) -> int:
+    return int(lib().convrot_linear_workspace_size(M, K))
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]) -> torch.Tensor:
+    if workspace is None:
+        return torch.empty((max(nbytes, 1),), dtype=torch.uint8, device=device)
+    if workspace.numel() * workspace.element_size() < nbytes:
+        raise ValueError("workspace too small")
+    return workspace
+
+
+def int8_linear(Q_x, s_x, Q_w=None, Q_w16=None, s_w=None, bias=None, Y=None,
+                workspace=None, stream=None) -> torch.Tensor:
+    """Y = float(Q_x Q_w^T) * s_x * s_w + bias, fp32 [M,N]."""
+    _need(Q_x, torch.int8, "Q_x")
+    _need(s_x, torch.float32, "s_x")
+    ref = Q_w16 if Q_w16 is not None else Q_w
+    if ref is None:
+        raise ValueError("Q_w or Q_w16 is required")
+    M, K = Q_x.shape
+    N = ref.shape[0]
+    if Q_w is not None:
+        _need(Q_w, torch.int8, "Q_w")
+    if Q_w16 is not None:
+        _need(Q_w16, torch.float16, "Q_w16")
+    if Y is None:
+        Y = torch.empty((M, N), dtype=torch.float32, device=Q_x.device)
+    ws = _workspace(int8_linear_workspace_size(M, N, K, Q_w16 is not None), Q_x.device, workspace)
+    _check(lib().int8_linear(_ptr(Q_x), _ptr(s_x), M, K, _ptr(Q_w), _ptr(Q_w16), _ptr(s_w), _ptr(bias),
+                             N, _ptr(Y), _ptr(ws), ws.numel(), _stream(stream)), "int8_linear")
+    return Y
+
+
+def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None) -> torch.Tensor:
+    """Raw int32 A = Q_x Q_w^T through the tensor-core GEMM."""
+    _need(Q_x, torch.int8, "Q_x")
+    ref = Q_w16 if Q_w16 is not None else Q_w
+    M, K = Q_x.shape
+    N = ref.shape[0]
+    if A is None:
+        A = torch.empty((M, N), dtype=torch.int32, device=Q_x.device)
+    ws = _workspace(int8_linear_workspace_size(M, N, K, Q_w16 is not None), Q_x.device, workspace)
+    _check(lib().int8_gemm_s32(_ptr(Q_x), M, K, _ptr(Q_w), _ptr(Q_w16), N, _ptr(A), _ptr(ws), ws.numel(),
+                               _stream(stream)), "int8_gemm_s32")
+    return A
+
+
+def make_weights(q16s: Sequence[torch.Tensor], scales: Sequence[Optional[torch.Tensor]],
+                 biases: Sequence[Optional[torch.Tensor]], Ys: Sequence[torch.Tensor]):
+    arr = (convrot_weight * len(q16s))()
+    for j, (q, s, b, y) in enumerate(zip(q16s, scales, biases, Ys)):
+        arr[j] = convrot_weight(_ptr(q), _ptr(s), _ptr(b), q.shape[0], _ptr(y))
+    return arr
+
+
+def convrot_linear(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
+                   scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
+                   Ys: Optional[List[torch.Tensor]] = None, workspace=None, stream=None,
+                   weights=None) -> List[torch.Tensor]:
+    """Pack X once, then every Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
+    ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
+    if weights is None:
+        weights = make_weights(q16s, scales, biases, Ys)
+    _check(lib().convrot_linear(_ptr(X), xd, M, K, G, weights, len(q16s), _ptr(ws), ws.numel(),
+                                _stream(stream)), "convrot_linear")
+    return Ys
+
+
+def convrot_pack_activations_f16(X: torch.Tensor, G: int, Q_x16: Optional[torch.Tensor] = None,
+                                 s_x: Optional[torch.Tensor] = None, stream=None):
+    """Pack X into the GEMM operand form: (Q_x16 fp16 codes [M,K], s_x f32 [M])."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    if Q_x16 is None:
+        Q_x16 = torch.empty((M, K), dtype=torch.float16, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _need(Q_x16, torch.float16, "Q_x16")
+    _need(s_x, torch.float32, "s_x")
+    _check(lib().convrot_pack_activations_f16(_ptr(X), xd, M, K, G, _ptr(Q_x16), _ptr(s_x), _stream(stream)),
+           "convrot_pack_activations_f16")
+    return Q_x16, s_x
+
+
+def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases,
+                          Ys=None, stream=None, weights=None):
+    """Grouped GEMM on an already packed activation (fp16 codes + row scales)."""
+    _need(Q_x16, torch.float16, "Q_x16")
+    _need(s_x, torch.float32, "s_x")
+    M, K = Q_x16.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=Q_x16.device) for q in q16s]
+    if weights is None:
+        weights = make_weights(q16s, scales, biases, Ys)
+    _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _stream(stream)),
+           "convrot_linear_packed")
+    return Ys
+
+
+def convrot_device_status(stream=None) -> int:
+    return int(lib().convrot_device_status(_stream(stream)))

@@ -1,0 +1,122 @@
+"""CPU checks of the C ABI: the library builds, loads and exports every entry
+point that include/convrot.h declares, and the host-side argument checks
+reject bad calls with the documented status codes before touching a GPU.
+(Fake device addresses are fine here: argument checks never dereference.)
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "convrot.h")
+
+
+@pytest.fixture(scope="session")
+def L():
+    from int8_hadamard_rotated_gb300 import build, ops
+    build.build()
+    return ops.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:int|size_t|const char\s*\*)\s+(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    names = set(declared_functions())
+    for n in ("convrot_prepare_weight", "convrot_pack_activations", "int8_linear",
+              "convrot_linear", "int8_gemm_s32", "convrot_linear_workspace_size",
+              "int8_linear_workspace_size", "convrot_device_status", "convrot_strerror",
+              "convrot_version", "convrot_last_cuda_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    from int8_hadamard_rotated_gb300 import ops
+    for name in declared_functions():
+        assert hasattr(L, name), name
+        assert name in ops.SIGNATURES, name
+
+
+def test_strerror_and_version(L):
+    assert L.convrot_version() >= 100
+    for code in range(11):
+        assert L.convrot_strerror(code)
+    assert b"unknown" in L.convrot_strerror(99)
+
+
+def test_workspace_sizes(L):
+    assert L.convrot_linear_workspace_size(4608, 3072) == 4608 * 3072 * 2 + ((4608 * 4 + 255) // 256) * 256
+    assert L.int8_linear_workspace_size(16, 128, 256, 1) == 16 * 256 * 2
+    assert L.int8_linear_workspace_size(16, 128, 256, 0) == 16 * 256 * 2 + 128 * 256 * 2
+
+
+# fake, 256-aligned, non-overlapping device addresses
+A0, A1, A2, A3, A4, A5 = (0x7f0000000000 + i * 0x10000000 for i in range(6))
+
+
+def test_pack_argument_checks(L):
+    from int8_hadamard_rotated_gb300 import ops
+    f = L.convrot_pack_activations
+    assert f(A0, ops.F32, 0, 256, 256, A1, A2, None) == ops.OK              # M = 0: no-op
+    assert f(None, ops.F32, 4, 256, 256, A1, A2, None) == ops.ERR_ARG
+    assert f(A0, 7, 4, 256, 256, A1, A2, None) == ops.ERR_ARG               # dtype
+    assert f(A0, ops.F32, -1, 256, 256, A1, A2, None) == ops.ERR_ARG
+    for G in (2, 8, 32, 128, 512, 4096, 0):
+        assert f(A0, ops.F32, 4, 4096, G, A1, A2, None) == ops.ERR_GROUP
+    assert f(A0, ops.F32, 4, 1280, 1024, A1, A2, None) == ops.ERR_GROUP     # 1024 does not divide 1280
+    assert f(A0, ops.F32, 4, 40, 4, A1, A2, None) == ops.ERR_ALIGN          # K % 16
+    assert f(A0 + 4, ops.F32, 4, 256, 256, A1, A2, None) == ops.ERR_ALIGN
+    assert f(A0, ops.F32, 4, 65536, 256, A1, A2, None) == ops.ERR_UNSUPPORTED
+    assert f(A0, ops.F32, 4, 256, 256, A0 + 256, A2, None) == ops.ERR_ALIAS  # Q_x inside X
+    assert f(A0, ops.F32, 4, 256, 256, A1, A1 + 512, None) == ops.ERR_ALIAS  # s_x inside Q_x
+
+
+def test_gemm_argument_checks(L):
+    from int8_hadamard_rotated_gb300 import ops
+    f = L.int8_linear
+    big = 1 << 40
+    assert f(A0, A1, 0, 256, A2, None, None, None, 128, A3, A4, big, None) == ops.OK
+    assert f(None, A1, 4, 256, A2, None, None, None, 128, A3, A4, big, None) == ops.ERR_ARG
+    assert f(A0, A1, 4, 256, None, None, None, None, 128, A3, A4, big, None) == ops.ERR_ARG
+    assert f(A0, A1, 4, 250, A2, None, None, None, 128, A3, A4, big, None) == ops.ERR_ALIGN
+    assert f(A0, A1, 4, 133152, A2, None, None, None, 128, A3, A4, big, None) == ops.ERR_OVERFLOW
+    assert f(A0, A1, 4, 256, A2, None, None, None, 128, A3, None, 0, None) == ops.ERR_WORKSPACE
+    assert f(A0, A1, 4, 256, A2, None, None, None, 128, A3, A4, 100, None) == ops.ERR_WORKSPACE
+    assert f(A0, A1, 4, 256, A2, None, None, None, 128, A0, A4, big, None) == ops.ERR_ALIAS
+    assert f(A0, A1, 4, 256, A2, None, None, None, 128, A3, A3 + 256, big, None) == ops.ERR_ALIAS
+
+
+def test_linear_argument_checks(L):
+    from int8_hadamard_rotated_gb300 import ops
+    f = L.convrot_linear
+    W = ops.convrot_weight
+    ws = (W * 2)(W(A1, A2, A3, 64, A4), W(A1 + 0x100000, None, None, 64, A5))
+    big = 1 << 40
+    assert f(A0, ops.F32, 16, 256, 256, ws, 0, A3 + 0x1000000, big, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 256, 256, ws, 9, A3 + 0x1000000, big, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 256, 128, ws, 2, A3 + 0x1000000, big, None) == ops.ERR_GROUP
+    assert f(A0, ops.F32, 16, 256, 256, ws, 2, None, 0, None) == ops.ERR_WORKSPACE
+    same = (W * 2)(W(A1, None, None, 64, A4), W(A1, None, None, 64, A4))
+    assert f(A0, ops.F32, 16, 256, 256, same, 2, A3 + 0x1000000, big, None) == ops.ERR_ALIAS
+
+
+def test_valid_call_without_gpu_reports_device(L):
+    """A well-formed call on a machine without an sm_103 GPU fails cleanly."""
+    import torch
+    from int8_hadamard_rotated_gb300 import ops
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert L.convrot_pack_activations(A0, ops.F32, 4, 256, 256, A1, A2, None) == ops.ERR_DEVICE
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from int8_hadamard_rotated_gb300 import ops
+    monkeypatch.setattr(ops, "_LIB", None)
+    monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        ops.lib()

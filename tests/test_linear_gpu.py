@@ -1,0 +1,119 @@
+"""GPU parity of the fused convrot linear (one pack, one grouped GEMM) against
+the oracle on the seeded workloads, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_hadamard_rotated_gb300 import workloads
+from gpu_common import dev, host
+from parity import assert_y, y_rel_err
+
+pytestmark = pytest.mark.gpu
+
+
+def prepared(ops, W, G):
+    Qw, s_w, Qw16 = ops.convrot_prepare_weight(dev(W), G)
+    return Qw, s_w, Qw16
+
+
+def run_linear(ops, X, Ws, bs, G):
+    preps = [prepared(ops, W, G) for W in Ws]
+    Ys = ops.convrot_linear(dev(X), G, [p[2] for p in preps], [p[1] for p in preps], [dev(b) for b in bs])
+    return [host(y) for y in Ys], [(host(p[0]), host(p[1])) for p in preps]
+
+
+def oracle_linear(X, Ws, bs, G, gpu_weights=None):
+    """Oracle Y. With gpu_weights, the oracle uses the GPU's weight codes so
+    that only the activation path is compared."""
+    out = []
+    for j, (W, b) in enumerate(zip(Ws, bs)):
+        if gpu_weights is None:
+            Qw, s_w = oracle.prepare_weight(W, G)
+        else:
+            Qw, s_w = gpu_weights[j]
+        out.append(oracle.linear(X, Qw, s_w, b, G))
+    return out
+
+
+def check_workload(ops, name):
+    w = workloads.get(name)
+    case = workloads.make_case(w)
+    Ys, gw = run_linear(ops, case.X, case.Ws, case.bs, w.G)
+    refs = oracle_linear(case.X, case.Ws, case.bs, w.G)
+    errs = [assert_y(y, r, f"{name} Y{j}") for j, (y, r) in enumerate(zip(Ys, refs))]
+    # with the GPU's own weight codes the only remaining difference is the
+    # rare +-1 activation code
+    refs2 = oracle_linear(case.X, case.Ws, case.bs, w.G, gpu_weights=gw)
+    for y, r in zip(Ys, refs2):
+        assert_y(y, r)
+    assert ops.convrot_device_status() == ops.OK
+    return errs
+
+
+def test_tiny(ops):
+    check_workload(ops, "tiny")
+
+
+def test_unet_fp16(ops):
+    check_workload(ops, "unet")
+
+
+def test_dit_qkv_shared_pack(ops):
+    check_workload(ops, "dit_qkv")
+
+
+def test_dit_mlp_pair(ops):
+    """Up linear, host GELU, repack, down linear. Stage-wise parity: the down
+    stage gets the same host GELU(Y_up_oracle) array on both sides."""
+    w = workloads.get("dit_mlp")
+    case = workloads.make_case(w)
+    G = w.G
+    (Y_up,), _ = run_linear(ops, case.X, case.Ws[:1], case.bs[:1], G)
+    Qw_up, sw_up = oracle.prepare_weight(case.Ws[0], G)
+    Y_up_ref = oracle.linear(case.X, Qw_up, sw_up, case.bs[0], G)
+    assert_y(Y_up, Y_up_ref, "mlp up")
+    H = oracle.gelu(Y_up_ref)
+    (Y_dn,), _ = run_linear(ops, H, case.Ws[1:], case.bs[1:], G)
+    Qw_dn, sw_dn = oracle.prepare_weight(case.Ws[1], G)
+    Y_dn_ref = oracle.linear(H, Qw_dn, sw_dn, case.bs[1], G)
+    assert_y(Y_dn, Y_dn_ref, "mlp down")
+    # end-to-end chain (informative): GPU up -> host GELU of the GPU output -> GPU down
+    (Y_chain,), _ = run_linear(ops, oracle.gelu(Y_up), case.Ws[1:], case.bs[1:], G)
+    assert y_rel_err(Y_chain, Y_dn_ref) < 1e-2
+
+
+@pytest.mark.parametrize("M,K,Ns,G", [
+    (1, 64, (1,), 64), (5, 256, (129, 7), 16), (300, 1024, (256, 130, 385), 1024),
+    (257, 1280, (64,), 4), (100, 48, (33,), 1),
+])
+def test_ragged_grouped(ops, M, K, Ns, G):
+    rng = workloads.rng_for(M + K + G)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=30.0)
+    Ws = [workloads.weights(rng, n, K) for n in Ns]
+    bs = [workloads.biases(rng, n) for n in Ns]
+    Ys, gw = run_linear(ops, X, Ws, bs, G)
+    refs = oracle_linear(X, Ws, bs, G, gpu_weights=gw)
+    for y, r in zip(Ys, refs):
+        assert_y(y, r)
+
+
+def test_optional_scale_and_bias(ops):
+    rng = workloads.rng_for(77)
+    X = workloads.activations(rng, 64, 256)
+    W = workloads.weights(rng, 96, 256)
+    Qw, s_w, Qw16 = prepared(ops, W, 256)
+    Y0, Y1 = ops.convrot_linear(dev(X), 256, [Qw16, Qw16], [None, s_w], [None, None])
+    Qx, s_x = oracle.pack(X, 256)
+    A = oracle.gemm_s32(Qx, host(Qw))
+    assert_y(host(Y0), oracle.reconstruct(A, s_x))
+    assert_y(host(Y1), oracle.reconstruct(A, s_x, host(s_w)))
+
+
+def test_alias_rejected(ops):
+    X = torch.randn(64, 256, device="cuda")
+    W = torch.randn(64, 256, device="cuda")
+    _, s_w, Qw16 = ops.convrot_prepare_weight(W, 256)
+    with pytest.raises(ops.ConvrotError) as e:
+        ops.convrot_linear(X, 256, [Qw16], [s_w], [None], Ys=[X.view(64, 256)])
+    assert e.value.status == ops.ERR_ALIAS

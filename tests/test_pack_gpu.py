@@ -1,0 +1,121 @@
+"""GPU parity of the pack kernel (rotation + row absmax + quantization) against
+the oracle, through the C ABI, on the workloads' seeded inputs and edge cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_hadamard_rotated_gb300 import workloads
+from gpu_common import dev, host
+from parity import assert_codes, assert_scales
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_pack(ops, X, G):
+    Q, s = ops.convrot_pack_activations(dev(X), G)
+    return host(Q), host(s)
+
+
+def check(ops, X, G, exact=False):
+    Q, s = gpu_pack(ops, X, G)
+    Qo, so = oracle.pack(X, G)
+    assert_scales(s, so)
+    n = assert_codes(Q, Qo)
+    if exact:
+        assert n == 0
+    return n
+
+
+def test_tiny_workload(ops):
+    case = workloads.make_case(workloads.get("tiny"))
+    check(ops, case.X, 256, exact=True)   # 1e-4 of 4096 codes rounds to zero mismatches
+
+
+@pytest.mark.parametrize("G", [4, 16, 64, 256, 1024])
+def test_pack_sweep_full_size(ops, G):
+    """4096 x 3072 fp32 with 0.5% channel outliers x30, every group size."""
+    case = workloads.make_case(workloads.get("pack_sweep"))
+    check(ops, case.X, G)
+
+
+def test_unet_fp16_input(ops):
+    case = workloads.make_case(workloads.get("unet"))
+    assert case.X.dtype == np.float16
+    check(ops, case.X, 256)
+
+
+def test_dit_input(ops):
+    case = workloads.make_case(workloads.get("dit_qkv"))
+    check(ops, case.X, 256)
+
+
+@pytest.mark.parametrize("G", [1, 4, 16, 64, 256, 1024])
+@pytest.mark.parametrize("M,Kmul", [(1, 1), (3, 2), (37, 3), (130, 5)])
+def test_ragged_shapes(ops, G, M, Kmul):
+    K = max(G, 16) * Kmul if G >= 16 else 16 * Kmul + (16 if G < 16 else 0)
+    rng = workloads.rng_for(G * 1000 + M * 10 + Kmul)
+    X = workloads.activations(rng, M, K, outlier_frac=0.02, outlier_mult=40.0)
+    check(ops, X, G)
+
+
+@pytest.mark.parametrize("K,G", [(16, 1), (48, 4), (80, 16), (1280, 256), (12288, 256),
+                                 (12288, 1024), (32768, 1024), (32768, 64)])
+def test_row_lengths(ops, K, G):
+    rng = workloads.rng_for(K + G)
+    X = workloads.activations(rng, 9, K, outlier_frac=0.01, outlier_mult=30.0)
+    check(ops, X, G)
+
+
+@pytest.mark.parametrize("G", [4, 16, 64, 256, 1024])
+def test_one_hot_rows(ops, G):
+    """x = c e_j: the closed form gives +-127 over the group, 0 elsewhere."""
+    K = 2048
+    X = np.zeros((4, K), np.float32)
+    X[0, 0] = 3.0
+    X[1, G + 5] = -40.0
+    X[2, K - 1] = 1000.0
+    X[3, 17] = 1e-20
+    Q, s = gpu_pack(ops, X, G)
+    Qo, so = oracle.pack(X, G)
+    np.testing.assert_array_equal(Q, Qo)
+    np.testing.assert_array_equal(s, so)
+
+
+def test_zero_and_constant_rows(ops):
+    K = 1024
+    X = np.zeros((5, K), np.float32)
+    X[1] = 2.5
+    X[2, ::2] = -1.0
+    X[4, 3] = 7.0
+    for G in (1, 4, 16, 64, 256, 1024):
+        Q, s = gpu_pack(ops, X, G)
+        Qo, so = oracle.pack(X, G)
+        np.testing.assert_array_equal(Q, Qo)
+        np.testing.assert_array_equal(s, so)
+        assert s[0] == 0 and s[3] == 0 and not Q[0].any() and not Q[3].any()
+
+
+def test_prepare_weight(ops):
+    case = workloads.make_case(workloads.get("unet"))
+    W = case.Ws[0]
+    Qw, s_w, Qw16 = ops.convrot_prepare_weight(dev(W), 256)
+    Qw, s_w, Qw16 = host(Qw), host(s_w), host(Qw16)
+    Qo, so = oracle.prepare_weight(W, 256)
+    assert_scales(s_w, so)
+    assert_codes(Qw, Qo)
+    np.testing.assert_array_equal(Qw16.astype(np.int32), Qw.astype(np.int32))
+
+
+def test_empty_batch(ops):
+    X = torch.zeros((0, 256), dtype=torch.float32, device="cuda")
+    Q, s = ops.convrot_pack_activations(X, 256)
+    assert Q.shape == (0, 256) and s.shape == (0,)
+
+
+def test_argument_errors_on_gpu(ops):
+    X = torch.zeros((4, 96), dtype=torch.float32, device="cuda")
+    with pytest.raises(ops.ConvrotError) as e:
+        ops.convrot_pack_activations(X, 64)
+    assert e.value.status == ops.ERR_GROUP
