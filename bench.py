@@ -1,0 +1,440 @@
+"""Benchmark of the convrot INT8 linear on one GB300 (or N independent replicas).
+
+A step is one pass of the whole hot path on the DiT attention-projection
+workload: X fp32 [4608, 3072] (1% outliers x40) is packed once with G = 256
+(rotation, row absmax, quantization) and one grouped tensor-core GEMM computes
+the three [3072, 3072] linears (Q, K, V) with the fused reconstruction.
+Weights are prepared offline (untimed). The step runs as the library's two
+stream-ordered calls (pack, grouped GEMM) so that CUDA events also time the
+dominant GEMM kernel alone; the e2e leg times the one-call convrot_linear API
+with host buffers, host<->device copies included.
+
+Metric: INT8-equivalent tera-operations per second (2*M*N*K summed over the
+linears, per step time). L2 is flushed (256 MiB write) before every timed
+step. Also reported: the pack-only sweep (X fp32 [4096, 3072], every G) in
+GB/s, the roofline of the GEMM kernel, SM clocks sampled during the timed
+region, and the CPU oracle timed on a bounded sample of the same workload.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from int8_hadamard_rotated_gb300 import workloads  # noqa: E402
+
+METRIC = "convrot INT8 linear TOPS (% INT8 TC peak); pack GB/s (% HBM peak)"
+UNIT = "TOPS"
+WORKLOAD = "dit_qkv"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def config_dict(w, n_gpus):
+    return {
+        "workload": f"{w.name}: X fp32 [{w.M},{w.K}] G={w.G} -> {len(w.Ns)} linears "
+                    f"[{w.Ns[0]},{w.K}] sharing one pack (grouped GEMM)",
+        "M": w.M, "K": w.K, "N": list(w.Ns), "G": w.G, "x_dtype": w.x_dtype,
+        "l2": "flushed before every timed step (256 MiB write)",
+        "parallelism": "replicas" if n_gpus > 1 else "single",
+    }
+
+
+def data_desc(w):
+    return (f"synthetic: seeded PCG64({w.seed}); X ~ N(0,1) with {w.outlier_frac:.0%} "
+            f"element outliers x{w.outlier_mult:g}; W ~ N(0,{w.w_std}); b ~ N(0,{w.b_std})")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline (bounded sample)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_seconds(case, w, rows, prepared):
+    import oracle
+    X = case.X[:rows]
+    t0 = time.perf_counter()
+    Qx, s_x = oracle.pack(X, w.G)
+    for (Qw, s_w), b in zip(prepared, case.bs):
+        oracle.reconstruct(oracle.gemm_s32(Qx, Qw), s_x, s_w, b)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(case, w, budget_s=10.0):
+    """Time the oracle as it stands on a sample of the workload's rows, growing
+    the sample until it takes about `budget_s` (or covers all rows)."""
+    import oracle
+    prepared = [oracle.prepare_weight(W, w.G) for W in case.Ws]
+    rows = 64
+    t = oracle_sample_seconds(case, w, rows, prepared)
+    while t < budget_s / 4 and rows < w.M:
+        rows = min(w.M, rows * 4)
+        t = oracle_sample_seconds(case, w, rows, prepared)
+    ops = 2.0 * rows * sum(w.Ns) * w.K
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    return {"value": ops / t / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"oracle pack + {len(w.Ns)} int32 GEMMs + reconstruction on the first "
+                      f"{rows} of {w.M} rows ({t:.2f} s; numpy/BLAS on all host cores)"}
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(self.gpu)], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons, power = [], None, set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    mx = float(parts[2])
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[5:9]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def gemm_traffic(kernel_src_hash):
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "gemm_dit_qkv_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        if d.get("gemm_cu_sha256") == kernel_src_hash:
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+def source_hash():
+    p = os.path.join(ROOT, "int8_hadamard_rotated_gb300", "csrc", "gemm.cu")
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def run_gpu(args, rank, world, local_rank):
+    import torch
+    from int8_hadamard_rotated_gb300 import build, ops
+
+    build.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    w = workloads.get(WORKLOAD)
+    case = workloads.make_case(w)
+    peaks, peak_kind = load_peaks()
+
+    # resident inputs and offline weight preparation (untimed)
+    X = torch.from_numpy(case.X).to(dev)
+    q16s, scales, biases = [], [], []
+    for W, b in zip(case.Ws, case.bs):
+        _, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), w.G)
+        q16s.append(q16)
+        scales.append(s_w)
+        biases.append(torch.from_numpy(b).to(dev))
+    Ys = [torch.empty((w.M, n), dtype=torch.float32, device=dev) for n in w.Ns]
+    Qx16 = torch.empty((w.M, w.K), dtype=torch.float16, device=dev)
+    s_x = torch.empty((w.M,), dtype=torch.float32, device=dev)
+    wdesc = ops.make_weights(q16s, scales, biases, Ys)
+    L = ops.lib()
+    sp = stream.cuda_stream
+    flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
+
+    def step():
+        st = L.convrot_pack_activations_f16(X.data_ptr(), ops.F32, w.M, w.K, w.G,
+                                            Qx16.data_ptr(), s_x.data_ptr(), sp)
+        if st:
+            raise ops.ConvrotError(st, "pack")
+        return st
+
+    def gemm():
+        st = L.convrot_linear_packed(Qx16.data_ptr(), s_x.data_ptr(), w.M, w.K, wdesc, len(q16s), sp)
+        if st:
+            raise ops.ConvrotError(st, "gemm")
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+        gemm()
+    torch.cuda.synchronize()
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        ev[k][0].record(stream)
+        step()
+        ev[k][1].record(stream)
+        gemm()
+        ev[k][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - wall0
+    clocks = sampler.stop()
+    status = ops.convrot_device_status()
+    if status != ops.OK:
+        raise ops.ConvrotError(status, "device status")
+
+    step_ms = np.array([e[0].elapsed_time(e[2]) for e in ev])
+    pack_ms = np.array([e[0].elapsed_time(e[1]) for e in ev])
+    gemm_ms = np.array([e[1].elapsed_time(e[2]) for e in ev])
+    ms_step = float(step_ms.mean())
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    ops_step = float(w.gemm_ops)
+    value = world * ops_step / (ms_step * 1e-3) / 1e12
+
+    gemm_tflops = ops_step / (gemm_ms.mean() * 1e-3) / 1e12
+    peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    fused_pack_bytes = w.M * w.K * 4 + w.M * w.K * 2 + w.M * 4
+    roofline = {
+        "bound": "tensor", "kernel": "convrot_gemm_kernel (tcgen05 kind::f16, exact int32)",
+        "achieved": round(gemm_tflops, 2), "peak": peak_tf, "unit": "TFLOP/s",
+        "frac": round(gemm_tflops / peak_tf, 4),
+        "peak_kind": f"{peak_kind} bf16 dense burst (fp16 nominal = bf16 nominal)",
+        "ops_per_launch": int(ops_step),
+        "traffic": gemm_traffic(source_hash()),
+    }
+
+    # ---- e2e: one convrot_linear call with host buffers -------------------
+    X_host = torch.from_numpy(case.X).pin_memory()
+    Y_host = [torch.empty((w.M, n), dtype=torch.float32).pin_memory() for n in w.Ns]
+    Xd = torch.empty_like(X)
+    ws = torch.empty((ops.convrot_linear_workspace_size(w.M, w.K),), dtype=torch.uint8, device=dev)
+    wdesc2 = ops.make_weights(q16s, scales, biases, Ys)
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        Xd.copy_(X_host, non_blocking=True)
+        st = L.convrot_linear(Xd.data_ptr(), ops.F32, w.M, w.K, w.G, wdesc2, len(q16s),
+                              ws.data_ptr(), ws.numel(), sp)
+        if st:
+            raise ops.ConvrotError(st, "convrot_linear")
+        for yh, yd in zip(Y_host, Ys):
+            yh.copy_(yd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": world * ops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+           "h2d_bytes_per_step": int(X_host.numel() * 4),
+           "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in Y_host)),
+           "ms_per_step": e2e_ms, "api": "convrot_linear (one call) + pinned H2D/D2H copies"}
+    # check parity of the e2e output against the timed path's output
+    Yt = [y.clone() for y in Ys]
+    step(); gemm()
+    torch.cuda.synchronize()
+
+    # ---- pack-only sweep (X fp32 [4096, 3072], every G) -------------------
+    pw = workloads.get("pack_sweep")
+    pcase = workloads.make_case(pw)
+    Xp = torch.from_numpy(pcase.X).to(dev)
+    Qp = torch.empty((pw.M, pw.K), dtype=torch.int8, device=dev)
+    sp_x = torch.empty((pw.M,), dtype=torch.float32, device=dev)
+    pack_bytes = pw.M * pw.K * 4 + pw.M * pw.K + pw.M * 4
+    sweep = {}
+    reps = 20
+    for G in pw.groups:
+        for _ in range(3):
+            L.convrot_pack_activations(Xp.data_ptr(), ops.F32, pw.M, pw.K, G, Qp.data_ptr(), sp_x.data_ptr(), sp)
+        times = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            st = L.convrot_pack_activations(Xp.data_ptr(), ops.F32, pw.M, pw.K, G, Qp.data_ptr(),
+                                            sp_x.data_ptr(), sp)
+            b.record(stream)
+            if st:
+                raise ops.ConvrotError(st, "pack sweep")
+            times.append((a, b))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+        gbs = pack_bytes / (ms * 1e-3) / 1e9
+        sweep[str(G)] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    pack = {
+        "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
+        "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
+        "peak_kind": f"{peak_kind} HBM copy", "by_group": sweep,
+        "fused_step_pack": {"us": round(float(pack_ms.mean()) * 1e3, 2),
+                            "bytes": fused_pack_bytes,
+                            "GB/s": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9, 1)},
+    }
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8", "data": data_desc(w), "config": config_dict(w, world),
+        "roofline": roofline, "pack": pack, "e2e": e2e,
+        "gpu_launches": 2 * args.steps,
+        "clocks": clocks,
+        "timing": {"step_ms_median": float(np.median(step_ms)), "pack_us_mean": float(pack_ms.mean() * 1e3),
+                   "gemm_us_mean": float(gemm_ms.mean() * 1e3), "wall_s_timed_loop": wall},
+        "e2e_parity_max_abs_diff": float(max((a - b).abs().max().item() for a, b in zip(Yt, Ys))),
+    }
+    return result, case, w
+
+
+def run_reference(args, rank):
+    """The oracle as the reference arm: each step is the oracle on a bounded
+    sample (the first 256 rows) of the same workload."""
+    if rank != 0:
+        return None
+    import oracle
+    w = workloads.get(WORKLOAD)
+    case = workloads.make_case(w)
+    rows = 256
+    prepared = [oracle.prepare_weight(W, w.G) for W in case.Ws]
+    for _ in range(args.warmup):
+        oracle_sample_seconds(case, w, rows, prepared)
+    times = [oracle_sample_seconds(case, w, rows, prepared) for _ in range(args.steps)]
+    t = float(np.mean(times))
+    ops_step = 2.0 * rows * sum(w.Ns) * w.K
+    v = ops_step / t / 1e12
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    return {
+        "metric": METRIC, "value": v, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": data_desc(w),
+        "config": config_dict(w, 1), "impl": "reference",
+        "cpu_baseline": {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"oracle on the first {rows} of {w.M} rows per step"},
+        "e2e": {"value": v, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank)
+        if res is not None:
+            print(json.dumps(res), flush=True)
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res, case, w = run_gpu(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline(case, w)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

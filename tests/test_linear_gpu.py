@@ -117,3 +117,23 @@ def test_alias_rejected(ops):
     with pytest.raises(ops.ConvrotError) as e:
         ops.convrot_linear(X, 256, [Qw16], [s_w], [None], Ys=[X.view(64, 256)])
     assert e.value.status == ops.ERR_ALIAS
+
+
+def test_packed_entry_points_match_fused_call(ops):
+    """convrot_pack_activations_f16 writes the int8 pack's codes as fp16, and
+    convrot_linear_packed on them equals the one-call convrot_linear."""
+    w = workloads.get("unet")
+    case = workloads.make_case(w)
+    X = dev(case.X)
+    Q8, s8 = ops.convrot_pack_activations(X, w.G)
+    Q16, s16 = ops.convrot_pack_activations_f16(X, w.G)
+    np.testing.assert_array_equal(host(Q16).astype(np.int32), host(Q8).astype(np.int32))
+    np.testing.assert_array_equal(host(s16), host(s8))
+    _, s_w, Qw16 = ops.convrot_prepare_weight(dev(case.Ws[0]), w.G)
+    b = dev(case.bs[0])
+    (Ya,) = ops.convrot_linear(X, w.G, [Qw16], [s_w], [b])
+    (Yb,) = ops.convrot_linear_packed(Q16, s16, [Qw16], [s_w], [b])
+    np.testing.assert_array_equal(host(Ya), host(Yb))
+    # and the packed GEMM equals int8_linear on the int8 codes
+    Yc = ops.int8_linear(Q8, s8, Q_w16=Qw16, s_w=s_w, bias=b)
+    np.testing.assert_array_equal(host(Yc), host(Ya))
