@@ -75,7 +75,8 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed. Returns false
 // (after recording a timeout in *err_word) if it does not complete within
-// kWaitLimitNs, or early if `*abort_flag` (shared) is set by another thread.
+// kWaitLimitNs, or early if `*abort_flag` (shared; may be null) is set by
+// another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag, int* err_word) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -83,9 +84,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 63) {
-      if (*abort_flag) return false;
+      if (abort_flag && *abort_flag) return false;
       if (global_timer_ns() - t0 > kWaitLimitNs) {
-        *abort_flag = 1;
+        if (abort_flag) *abort_flag = 1;
         record_error(err_word, CONVROT_ERR_TIMEOUT);
         return false;
       }
@@ -117,6 +118,18 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
   return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 32-bit global stores carrying an L2 cache-policy hint.
+__device__ __forceinline__ void st_global_hint(float* ptr, float v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(ptr), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_global_hint(int32_t* ptr, int32_t v, uint64_t pol) {
+  asm volatile("st.global.L2::cache_hint.s32 [%0], %1, %2;" ::"l"(ptr), "r"(v), "l"(pol) : "memory");
 }
 __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
   uint64_t p;

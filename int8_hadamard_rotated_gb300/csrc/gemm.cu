@@ -60,6 +60,7 @@ constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
 constexpr int MAX_LIN = CONVROT_MAX_LINEARS;
 constexpr int COLS_PER_THREAD = BN / 2;   // two epilogue warpgroups split the columns
 constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
+constexpr int RASTER_BANDS = 8;       // activation bands per raster group
 
 static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
@@ -95,10 +96,19 @@ struct TileCoord {
   int lin, wt, xt;
 };
 
+// Raster order: tiles are taken in groups of RASTER_BANDS activation bands;
+// inside a group, consecutive tiles walk the bands of one weight tile before
+// moving to the next weight tile (of the same or the next linear). The ~152
+// tiles in flight then cover ~RASTER_BANDS bands x ~152/RASTER_BANDS weight
+// tiles, which stay in L2 while the group is swept.
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
+  const int per_group = RASTER_BANDS * p.n_wtiles;
+  const int g = t / per_group;
+  const int idx = t - g * per_group;
+  const int gm = min(RASTER_BANDS, p.n_xtiles - g * RASTER_BANDS);
+  const int w = idx / gm;
   TileCoord c;
-  c.xt = t / p.n_wtiles;
-  const int w = t - c.xt * p.n_wtiles;
+  c.xt = g * RASTER_BANDS + (idx - w * gm);
   int j = 0;
 #pragma unroll 1
   while (j + 1 < p.n_lin && w >= p.wtile_start[j + 1]) ++j;
@@ -154,11 +164,10 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
 
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
-      const uint64_t pol_x = l2_policy_evict_last();
+      const uint64_t pol_x = l2_policy_evict_normal();
       const uint64_t pol_w = l2_policy_evict_normal();
-      int issued[STAGES];
-      for (int s = 0; s < STAGES; ++s) issued[s] = 0;
       uint32_t stage = 0, phase = 0;
+      uint32_t n_issued = 0;  // stage loads issued so far (stage = n % STAGES)
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
         const TileCoord c = decode_tile(p, t);
@@ -169,16 +178,16 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           uint8_t* sx = sw + W_TILE_BYTES;
           tma_load_2d(sw, &p.tmap_w[c.lin], &full[stage], kb * BK, c.wt * BM, pol_w);
           tma_load_2d(sx, &p.tmap_x, &full[stage], kb * BK, c.xt * BN, pol_x);
-          ++issued[stage];
+          ++n_issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       // No copy may land after the CTA exits: wait (bounded) for the last
       // phase of every stage that was ever filled.
-      for (int s = 0; s < STAGES; ++s)
-        if (issued[s] > 0) {
-          volatile int no_abort = 0;
-          mbar_wait(&full[s], static_cast<uint32_t>((issued[s] - 1) & 1), &no_abort, err);
+      for (uint32_t s = 0; s < STAGES; ++s)
+        if (n_issued > s) {
+          const uint32_t uses = (n_issued - 1 - s) / STAGES + 1;  // times stage s was filled
+          mbar_wait(&full[s], (uses - 1) & 1u, nullptr, err);
         }
     }
     __syncwarp();
@@ -217,12 +226,12 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       }
       // all issued MMAs complete before TMEM is released
       mma_commit(drain);
-      volatile int no_abort = 0;
-      mbar_wait(drain, 0, &no_abort, err);
+      mbar_wait(drain, 0, nullptr, err);
     }
     __syncwarp();
   } else {
     // ------------------------------ epilogue ------------------------------
+    const uint64_t pol_y = l2_policy_evict_first();
     const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
     const int half = warp >> 2;               // activation columns half*128 .. +127
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
@@ -261,7 +270,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
 #pragma unroll
           for (int i = 0; i < COLS_PER_THREAD; ++i) {
             const int r = r0 + i;
-            if (r < p.M) A[static_cast<int64_t>(r) * N + o] = acc[i];
+            if (r < p.M) st_global_hint(A + static_cast<int64_t>(r) * N + o, acc[i], pol_y);
           }
         } else {
           float* Y = static_cast<float*>(p.out[c.lin]);
@@ -277,7 +286,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
               float y = __fmul_rn(__int2float_rn(acc[i]), __ldg(p.s_x + r));
               if (sw_ptr) y = __fmul_rn(y, sw);
               if (b_ptr) y = __fadd_rn(y, bb);
-              __stcs(Y + static_cast<int64_t>(r) * N + o, y);
+              st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
             }
           }
         }

@@ -119,3 +119,39 @@ def test_argument_errors_on_gpu(ops):
     with pytest.raises(ops.ConvrotError) as e:
         ops.convrot_pack_activations(X, 64)
     assert e.value.status == ops.ERR_GROUP
+
+
+def test_rounding_ties_and_neighbours(ops):
+    """Quotients exactly at k + 1/2 (round half to even) and one ulp either
+    side, plus quotients that land within a few ulp of a half-integer after
+    an inexact scale: the quantizer must take the IEEE-division decision."""
+    K = 256
+    rows = []
+    # s = 1 exactly (row max 127): x / s = x
+    base = np.zeros(K, np.float32)
+    base[0] = 127.0
+    ks = np.arange(-60, 60, dtype=np.float32)
+    ties = ks + np.float32(0.5)
+    r = base.copy(); r[1:1 + len(ties)] = ties; rows.append(r)
+    r = base.copy(); r[1:1 + len(ties)] = np.nextafter(ties, np.float32(np.inf)); rows.append(r)
+    r = base.copy(); r[1:1 + len(ties)] = np.nextafter(ties, np.float32(-np.inf)); rows.append(r)
+    # inexact scales: x = (k + 1/2) * s rounded to fp32, for several row maxima
+    for amax in (100.0, 3.3, 0.07, 12345.678):
+        s = np.float32(np.float32(amax) / np.float32(127))
+        r = np.zeros(K, np.float32)
+        r[0] = np.float32(amax)
+        vals = (ks + np.float32(0.5)) * s
+        r[1:1 + len(vals)] = vals
+        r[1 + len(vals):1 + 2 * len(vals)] = np.nextafter(vals, np.float32(np.inf))
+        rows.append(r)
+    X = np.stack(rows).astype(np.float32)
+    Q, s = gpu_pack(ops, X, 1)
+    Qo, so = oracle.pack(X, 1)
+    np.testing.assert_array_equal(s, so)
+    np.testing.assert_array_equal(Q, Qo)
+    # the same rows through a rotation (G = 4): still identical decisions
+    # whenever the rotated values agree bit for bit
+    Q4, s4 = gpu_pack(ops, X, 4)
+    Qo4, so4 = oracle.pack(X, 4)
+    assert_scales(s4, so4)
+    assert_codes(Q4, Qo4)
