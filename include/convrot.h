@@ -70,7 +70,10 @@ typedef enum convrot_status {
                                   convrot_device_status) */
   CONVROT_ERR_CUDA = 9,        /* a CUDA runtime call failed or a launch error;
                                   convrot_last_cuda_error() gives the code */
-  CONVROT_ERR_DEVICE = 10      /* the current device is not an sm_103 GPU */
+  CONVROT_ERR_DEVICE = 10,     /* the current device is not an sm_103 GPU */
+  CONVROT_ERR_SCRATCH = 11     /* the packed activation does not fit in the
+                                  library's fixed scratch array
+                                  (convrot_linear_noalloc) */
 } convrot_status;
 
 /* Element type of the floating-point activation input X. */
@@ -204,6 +207,34 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
  */
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
                           const convrot_weight* weights, int n_weights, void* stream);
+
+/* Size of the fixed device array that convrot_linear_noalloc uses (32 MiB). */
+#define CONVROT_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * convrot_linear_noalloc -- convrot_linear for callers that cannot allocate
+ * device memory: a plugin that a host framework hands only its input and
+ * output buffers, or a latency-bound loop where cudaMalloc (which can
+ * synchronize the device) is not allowed. The pages have no counterpart; this
+ * entry point is a property of this library, not of the method.
+ *   Arguments and results as convrot_linear, without the workspace: the
+ *   packed activation lives in one library-owned device array of
+ *   CONVROT_NOALLOC_SCRATCH_BYTES bytes per GPU, held by every GPU that loads
+ *   the library until the process exits. It must hold
+ *   round256(M*K*2) + round256(M*4) bytes (round256 = round up to a multiple
+ *   of 256), e.g. M = 4608, K = 3072 fits; larger calls return
+ *   CONVROT_ERR_SCRATCH without launching anything.
+ * The call allocates nothing. Its first call on a device looks up the array's
+ * device address (cudaGetSymbolAddress), so make that first call before any
+ * stream capture. Every call on a device shares the one array: calls that
+ * overlap on the GPU (different streams, or host threads sharing a device)
+ * race and must be serialized by the caller.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_UNSUPPORTED,
+ *         ERR_SCRATCH, ERR_CUDA.
+ */
+int convrot_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, int G,
+                           const convrot_weight* weights, int n_weights,
+                           void* stream);
 
 /*
  * convrot_device_status -- synchronizes `stream`, then returns and clears the

@@ -59,9 +59,7 @@ int read_and_clear_device_error(cudaStream_t stream);  // gemm.cu
 
 }  // namespace convrot
 
-using namespace convrot;
-
-namespace {
+namespace convrot {
 
 bool valid_group(int G, int64_t K) {
   if (G < 1 || G > 1024) return false;
@@ -73,6 +71,12 @@ bool valid_group(int G, int64_t K) {
 size_t round256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }
 
 int check_device() { return device_is_sm103() ? CONVROT_OK : CONVROT_ERR_DEVICE; }
+
+}  // namespace convrot
+
+using namespace convrot;
+
+namespace {
 
 int pack_checks(const void* X, int x_dtype, int64_t M, int64_t K, int G, const void* Q, size_t q_esz,
                 const float* s);
@@ -96,6 +100,7 @@ const char* convrot_strerror(int status) {
     case CONVROT_ERR_TIMEOUT: return "a device-side wait timed out";
     case CONVROT_ERR_CUDA: return "CUDA runtime error";
     case CONVROT_ERR_DEVICE: return "the current device is not an sm_103 GPU";
+    case CONVROT_ERR_SCRATCH: return "packed activation larger than the fixed scratch (CONVROT_NOALLOC_SCRATCH_BYTES)";
     default: return "unknown status";
   }
 }
@@ -210,7 +215,7 @@ int int8_gemm_s32(const int8_t* Q_x, int64_t M, int64_t K,
 
 }  // extern "C"
 
-namespace {
+namespace convrot {
 
 // Checks of the weight descriptors against each other and against the
 // activation-side arrays [in0, in0+n0) and [in1, in1+n1).
@@ -262,6 +267,10 @@ int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
   if (n == 0) return CONVROT_OK;
   return launch_gemm(x16, s_x, M, K, lins, n, false, s);
 }
+
+}  // namespace convrot
+
+namespace {
 
 int pack_checks(const void* X, int x_dtype, int64_t M, int64_t K, int G, const void* Q, size_t q_esz,
                 const float* s) {

@@ -233,6 +233,13 @@ inline bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+// G is 4^n with 1 <= G <= 1024 and divides K.
+bool valid_group(int G, int64_t K);
+// b rounded up to a multiple of 256.
+size_t round256(size_t b);
+// CONVROT_OK on an sm_103 device, else CONVROT_ERR_DEVICE.
+int check_device();
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count();
 // Whether the current device is sm_103 (cached per device).
@@ -262,5 +269,19 @@ struct GemmLinear {
 // out_j = epilogue(x16 . w16_j^T) for every linear j; raw_s32 selects int32 A.
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream);
+
+// ---------------------------------------------------------------------------
+// host-side checks and the grouped launch shared by the entry points (api.cu)
+// ---------------------------------------------------------------------------
+
+// n_weights in [1, CONVROT_MAX_LINEARS]; every non-empty descriptor has q16 and Y.
+int check_weight_list(const convrot_weight* weights, int n_weights);
+// Alignment and aliasing of the weight descriptors against each other and
+// against the activation-side arrays [in0, in0+n0) and [in1, in1+n1).
+int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64_t K,
+                  const void* in0, size_t n0, const void* in1, size_t n1);
+// One grouped GEMM over the non-empty linears, on packed fp16 codes + s_x.
+int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
+                   const convrot_weight* weights, int n_weights, cudaStream_t s);
 
 }  // namespace convrot

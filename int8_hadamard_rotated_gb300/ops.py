@@ -30,12 +30,14 @@ ERR_UNSUPPORTED = 7
 ERR_TIMEOUT = 8
 ERR_CUDA = 9
 ERR_DEVICE = 10
+ERR_SCRATCH = 11
 
 F32 = 0
 F16 = 1
 MAX_LINEARS = 8
 PACK_MAX_K = 32768
 MAX_K = 133144
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
 class ConvrotError(RuntimeError):
@@ -70,6 +72,7 @@ SIGNATURES = {
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
     "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
+    "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_device_status": (_I, [_VP]),
 }
 
@@ -266,6 +269,27 @@ def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, 
         weights = make_weights(q16s, scales, biases, Ys)
     _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _stream(stream)),
            "convrot_linear_packed")
+    return Ys
+
+
+def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
+                           scales: Sequence[Optional[torch.Tensor]],
+                           biases: Sequence[Optional[torch.Tensor]],
+                           Ys: Optional[List[torch.Tensor]] = None, stream=None,
+                           weights=None) -> List[torch.Tensor]:
+    """convrot_linear without a workspace, for callers that cannot allocate
+    device memory: the packed activation lives in the library's fixed device
+    array (NOALLOC_SCRATCH_BYTES per GPU). Pass preallocated Ys to make the
+    whole call allocation-free; calls that overlap on the GPU race."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
+    if weights is None:
+        weights = make_weights(q16s, scales, biases, Ys)
+    _check(lib().convrot_linear_noalloc(_ptr(X), xd, M, K, G, weights, len(q16s), _stream(stream)),
+           "convrot_linear_noalloc")
     return Ys
 
 
