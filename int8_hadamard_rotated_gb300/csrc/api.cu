@@ -55,7 +55,8 @@ bool device_is_sm103() {
   return d && d->is_sm103 == 1;
 }
 
-int read_and_clear_device_error(cudaStream_t stream);  // gemm.cu
+int read_and_clear_device_error(cudaStream_t stream);  // gemm.cu: syncs, then the GEMM's word
+int read_and_clear_pack_error();                       // pack.cu: the pack kernels' word
 
 }  // namespace convrot
 
@@ -353,7 +354,9 @@ int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
 
 int convrot_device_status(void* stream) {
   if (int st = check_device()) return st;
-  return read_and_clear_device_error(static_cast<cudaStream_t>(stream));
+  const int gemm_st = read_and_clear_device_error(static_cast<cudaStream_t>(stream));
+  const int pack_st = read_and_clear_pack_error();
+  return gemm_st != CONVROT_OK ? gemm_st : pack_st;
 }
 
 }  // extern "C"

@@ -32,20 +32,33 @@
 // consecutive elements (index bits 0-3 in registers). For G >= 64 the four
 // units are the four values of the group's top base-4 digit (registers); the
 // digits between bit 4 and the top digit live on G/64 consecutive lanes
-// (shuffles). A row is handled by ceil(K/64) threads of one CTA.
+// (shuffles). For G <= 16 every unit is a whole number of groups, so units
+// are dealt out to the row's threads round-robin. A row is handled by
+// ceil(K/64) threads of one CTA; the row absmax is a warp-segment shuffle
+// reduction plus one shared-memory 64-bit atomic max per segment, tagged with
+// the iteration so no reset is needed.
 //
-// Pipeline. CTAs are persistent over blocks of rows. Each thread prefetches
-// its next block with 16-byte cp.async copies into a private, lane-interleaved
-// shared-memory layout ([stage][chunk][thread], conflict-free), so one block's
-// loads are in flight while the previous one is rotated and quantized. The row
-// absmax is a warp-segment shuffle reduction plus one shared-memory 64-bit
-// atomic max per segment, tagged with the iteration so no reset is needed.
+// Two kernels share that arithmetic:
+//   pack_tma_kernel (rows whose length is a whole number of 128-byte lines):
+//     persistent CTAs over blocks of R rows. One thread streams blocks into a
+//     ring of shared-memory stages with 3-D TMA tensor copies (128-byte
+//     swizzle, so the threads' 16-byte reads of their units spread over the
+//     banks); the codes of a block are staged in shared memory and written
+//     back with one bulk copy, while the next blocks' loads are in flight.
+//   pack_kernel (any K % 16 == 0, rows up to 32768 elements): per-thread
+//     16-byte cp.async copies into a lane-interleaved two-stage buffer and
+//     direct 16-byte stores of the codes.
 #include "common.cuh"
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 namespace convrot {
+
+// Sticky device error word of the pack kernels (timeouts of bounded waits).
+__device__ int g_pack_error = 0;
+
 namespace {
 
 template <int G>
@@ -184,6 +197,202 @@ __device__ __forceinline__ void unit_to_f32<__half>(const uint4 (&c)[2], float (
   }
 }
 
+
+// ---- the per-thread arithmetic shared by both kernels ------------------------
+
+// Per-lane constants of the cross-lane butterflies (G = 256, 1024). The true
+// value of a held number is rho * held. A butterfly on lane bit b maps
+//   true' = (bit ? -1 : 1) * true(self) + true(partner)
+// to held' = fma(held, coef[b], held(partner)) with
+// coef[b] = s_b * rho(self) * rho(partner), and rho'(self) = rho(partner);
+// the coefficients are per-lane constants. `flip` is the residual rho of the
+// held values times the lane's output sign.
+template <int G>
+struct LaneSigns {
+  float coef[Geo<G>::kLaneBits > 0 ? Geo<G>::kLaneBits : 1];
+  int flip;
+};
+
+template <int G>
+__device__ __forceinline__ LaneSigns<G> lane_signs(int li) {
+  LaneSigns<G> ls;
+  int rho_mask = 0;
+#pragma unroll
+  for (int b = 0; b < Geo<G>::kLaneBits; ++b) {
+    const int pli = li ^ (1 << b);
+    const int rs = lane_sign<G>(li ^ rho_mask);
+    const int rp = lane_sign<G>(pli ^ rho_mask);
+    const int sb = (li >> b) & 1;
+    ls.coef[b] = ((sb ^ rs ^ rp) & 1) ? -1.0f : 1.0f;
+    rho_mask |= (1 << b);
+  }
+  if (Geo<G>::kLaneBits == 0) ls.coef[0] = 1.0f;
+  ls.flip = (Geo<G>::kLaneBits > 0) ? (lane_sign<G>(li ^ rho_mask) ^ lane_sign<G>(li)) : 0;
+  return ls;
+}
+
+// Input signs and every butterfly of W_G on the 64 values a thread holds
+// (in place). The result is 2^n X_rot up to the lane sign `flip`, with the
+// output signs of the register digits still to be applied.
+template <int G>
+__device__ __forceinline__ void rotate64(float (&v)[4][16], const LaneSigns<G>& ls) {
+  using C = Geo<G>;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int p = 0; p < 16; ++p)
+      if (static_sign<G>(j, p)) v[j][p] = -v[j][p];
+
+  // bit 0 scalar, then packed pairs (p, p+1)
+  if (C::kUnitBits >= 1) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int p = 0; p < 16; p += 2) {
+        const float a = v[j][p], c = v[j][p + 1];
+        v[j][p] = a + c;
+        v[j][p + 1] = a - c;
+      }
+  }
+  unsigned long long w[4][8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) w[j][h] = f2pack(v[j][2 * h], v[j][2 * h + 1]);
+#pragma unroll
+  for (int b = 1; b < C::kUnitBits; ++b) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int h = 0; h < 8; ++h)
+        if (!((h >> (b - 1)) & 1)) bfly2(w[j][h], w[j][h | (1 << (b - 1))]);
+  }
+  if (C::kUnitDigit) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b)
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (!((j >> b) & 1))
+#pragma unroll
+          for (int h = 0; h < 8; ++h) bfly2(w[j][h], w[j | (1 << b)][h]);
+  }
+#pragma unroll
+  for (int b = 0; b < C::kLaneBits; ++b) {
+    const unsigned long long cc = f2pack(ls.coef[b], ls.coef[b]);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        float a0, a1;
+        f2unpack(w[j][h], a0, a1);
+        const float u0 = __shfl_xor_sync(0xffffffffu, a0, 1 << b);
+        const float u1 = __shfl_xor_sync(0xffffffffu, a1, 1 << b);
+        w[j][h] = fma2(w[j][h], cc, f2pack(u0, u1));
+      }
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int h = 0; h < 8; ++h) f2unpack(w[j][h], v[j][2 * h], v[j][2 * h + 1]);
+}
+
+__device__ __forceinline__ float absmax64(const float (&v)[4][16]) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int p = 0; p < 16; ++p) amax = fmaxf(amax, fabsf(v[j][p]));
+  return amax;
+}
+
+// Divisor of the held values: d = s * 2^n (negated when the lane's held values
+// carry a residual sign), so that z / d = X_rot / s as real numbers.
+template <int G>
+__device__ __forceinline__ float held_divisor(float s, int flip) {
+  const float d = s * Geo<G>::kScale;
+  return flip ? -d : d;
+}
+
+// Codes of unit j (rounded quotients as integer-valued floats), in output order.
+template <int G>
+__device__ __forceinline__ void quantize_unit(const float (&vj)[16], int j, float d, float rcp, bool zero_row,
+                                              float (&qr)[16]) {
+  const unsigned long long rcp2 = f2pack(rcp, rcp);
+  const unsigned long long magic2 = f2pack(kMagic, kMagic);
+  bool near_half = false;
+#pragma unroll
+  for (int p = 0; p < 16; p += 2) {
+    // output sign of the register digits (the same function as the input sign)
+    const float z0 = static_sign<G>(j, p) ? -vj[p] : vj[p];
+    const float z1 = static_sign<G>(j, p + 1) ? -vj[p + 1] : vj[p + 1];
+    const unsigned long long q = mul2(f2pack(z0, z1), rcp2);
+    const unsigned long long t2 = sub2(add2(q, magic2), magic2);
+    const unsigned long long e = sub2(q, t2);
+    float e0, e1, t0, t1;
+    f2unpack(e, e0, e1);
+    f2unpack(t2, t0, t1);
+    near_half |= (fabsf(e0) > kNearHalf) | (fabsf(e1) > kNearHalf);
+    qr[out_pos<G>(p)] = t0;
+    qr[out_pos<G>(p + 1)] = t1;
+  }
+  if (near_half) {
+    // the exact IEEE quotient for the values near a rounding boundary
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+      const float z = static_sign<G>(j, p) ? -vj[p] : vj[p];
+      const float q = z * rcp;
+      const float tt = (q + kMagic) - kMagic;
+      if (fabsf(q - tt) > kNearHalf) qr[out_pos<G>(p)] = rintf(__fdiv_rn(z, d));
+    }
+  }
+  if (zero_row) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) qr[p] = 0.0f;
+  }
+}
+
+// 16 codes -> 16 int8 bytes (one 16-byte vector).
+__device__ __forceinline__ uint4 codes_i8(const float (&qr)[16]) {
+  uint32_t b[16];
+#pragma unroll
+  for (int p = 0; p < 16; ++p) b[p] = __float_as_uint(qr[p] + kMagic);  // low byte = code
+  uint4 wv;
+  wv.x = pack4_low_bytes(b[0], b[1], b[2], b[3]);
+  wv.y = pack4_low_bytes(b[4], b[5], b[6], b[7]);
+  wv.z = pack4_low_bytes(b[8], b[9], b[10], b[11]);
+  wv.w = pack4_low_bytes(b[12], b[13], b[14], b[15]);
+  return wv;
+}
+
+// 16 codes -> 16 binary16 integers (two 16-byte vectors).
+__device__ __forceinline__ void codes_f16(const float (&qr)[16], uint4& lo, uint4& hi) {
+  uint32_t hw[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    __half2 h = __floats2half2_rn(qr[2 * k], qr[2 * k + 1]);
+    hw[k] = *reinterpret_cast<uint32_t*>(&h);
+  }
+  lo = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  hi = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+}
+
+// Unit of the row held in register slot j by a thread (gi, li); and the unit
+// its codes are written to (the bit-swap permutation P_G acts on the digits
+// above bit 3 here, and on bits 0-3 through out_pos).
+template <int G>
+__device__ __forceinline__ int in_unit_grouped(int gi, int li, int j) {
+  return gi * 4 * Geo<G>::kTPG + j * Geo<G>::kTPG + li;
+}
+template <int G>
+__device__ __forceinline__ int out_unit(int u, int gi, int li, int j) {
+  if (G <= 16) return u;
+  if (G == 64) return gi * 4 + swap2(j);
+  if (G == 256) return gi * 16 + swap2(j) * 4 + swap2(li);
+  return gi * 64 + swap2(j) * 16 + swap_digit_bits4(li);
+}
+
+// ---- pack_kernel: the general path (per-thread cp.async) ---------------------
+
 // One CTA handles `rpc` rows with `tpr` threads each per block, persistently.
 template <int G, typename TIn, int OUT>
 __global__ void __launch_bounds__(kMaxThreads)
@@ -213,7 +422,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     const TIn* xrow = X + (active ? row : 0) * static_cast<int64_t>(K);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int u = gi * 4 * C::kTPG + j * C::kTPG + li;
+      const int u = in_unit_grouped<G>(gi, li, j);
       const bool ok = active && u < units;
       const TIn* src = ok ? xrow + 16 * u : X;
 #pragma unroll
@@ -226,21 +435,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     }
   };
 
-  // lane-sign bookkeeping for the cross-lane butterflies (see below)
-  float lane_coef[C::kLaneBits > 0 ? C::kLaneBits : 1];
-  int rho_mask = 0;
-#pragma unroll
-  for (int b = 0; b < C::kLaneBits; ++b) {
-    const int pli = li ^ (1 << b);
-    const int rs = lane_sign<G>(li ^ rho_mask);
-    const int rp = lane_sign<G>(pli ^ rho_mask);
-    const int sb = (li >> b) & 1;
-    lane_coef[b] = ((sb ^ rs ^ rp) & 1) ? -1.0f : 1.0f;
-    rho_mask |= (1 << b);
-  }
-  // residual lane sign of the held values, times the output lane sign
-  const int lane_flip = (C::kLaneBits > 0) ? (lane_sign<G>(li ^ rho_mask) ^ lane_sign<G>(li)) : 0;
-
+  const LaneSigns<G> ls = lane_signs<G>(li);
   // aligned lane segments of gcd(tpr, 32) lanes never straddle two rows
   const int seg = tpr & -tpr;
   const int segw = seg < 32 ? seg : 32;
@@ -267,7 +462,6 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     const int64_t row = blk * rpc + lr;
     const bool active = in_cta_row && row < M;
 
-    // ---- load own data from shared memory --------------------------------
     float v[4][16];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -276,78 +470,9 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
       for (int k = 0; k < CPU; ++k) c[k] = stage_buf[(stage * CH + j * CPU + k) * nth + tid];
       unit_to_f32<TIn>(c, v[j]);
     }
+    rotate64<G>(v, ls);
 
-    // ---- input signs of the register digits ------------------------------
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int p = 0; p < 16; ++p)
-        if (static_sign<G>(j, p)) v[j][p] = -v[j][p];
-
-    // ---- butterflies: bit 0 scalar, then packed pairs (p, p+1) ------------
-    if (C::kUnitBits >= 1) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int p = 0; p < 16; p += 2) {
-          const float a = v[j][p], c = v[j][p + 1];
-          v[j][p] = a + c;
-          v[j][p + 1] = a - c;
-        }
-    }
-    unsigned long long w[4][8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int h = 0; h < 8; ++h) w[j][h] = f2pack(v[j][2 * h], v[j][2 * h + 1]);
-#pragma unroll
-    for (int b = 1; b < C::kUnitBits; ++b) {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int h = 0; h < 8; ++h)
-          if (!((h >> (b - 1)) & 1)) bfly2(w[j][h], w[j][h | (1 << (b - 1))]);
-    }
-    if (C::kUnitDigit) {
-#pragma unroll
-      for (int b = 0; b < 2; ++b)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if (!((j >> b) & 1))
-#pragma unroll
-            for (int h = 0; h < 8; ++h) bfly2(w[j][h], w[j | (1 << b)][h]);
-    }
-    // ---- butterflies across lanes ----------------------------------------
-    // The true value is rho * held. A butterfly on lane bit b maps
-    //   true' = (bit ? -1 : 1) * true(self) + true(partner)
-    // to held' = fma(held, s_b * rho(self) * rho(partner), held(partner)) and
-    // rho'(self) = rho(partner); the coefficients are per-lane constants.
-#pragma unroll
-    for (int b = 0; b < C::kLaneBits; ++b) {
-      const unsigned long long cc = f2pack(lane_coef[b], lane_coef[b]);
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          float a0, a1;
-          f2unpack(w[j][h], a0, a1);
-          const float u0 = __shfl_xor_sync(0xffffffffu, a0, 1 << b);
-          const float u1 = __shfl_xor_sync(0xffffffffu, a1, 1 << b);
-          w[j][h] = fma2(w[j][h], cc, f2pack(u0, u1));
-        }
-    }
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int h = 0; h < 8; ++h) f2unpack(w[j][h], v[j][2 * h], v[j][2 * h + 1]);
-
-    // ---- row absmax ----------------------------------------------------------
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < 4; ++j)
-#pragma unroll
-      for (int p = 0; p < 16; ++p) amax = fmaxf(amax, fabsf(v[j][p]));
-    unsigned abits = __float_as_uint(amax);
+    unsigned abits = __float_as_uint(absmax64(v));
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1)
       if (off < segw) abits = max(abits, __shfl_xor_sync(0xffffffffu, abits, off));
@@ -361,85 +486,255 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     // X_rot = z * 2^-n exactly, so max |X_rot| = amax_z * 2^-n.
     const float s = __fdiv_rn(amax_z * C::kInvScale, 127.0f);
     if (t == 0) scales[row] = s;
-    // z / (s * 2^n) equals X_rot / s as a real number, hence the same rounded quotient.
-    float d = s * C::kScale;
-    if (lane_flip) d = -d;
+    const float d = held_divisor<G>(s, ls.flip);
     const bool zero_row = (s == 0.0f);
     const float rcp = zero_row ? 0.0f : __frcp_rn(d);
-    const unsigned long long rcp2 = f2pack(rcp, rcp);
-    const unsigned long long magic2 = f2pack(kMagic, kMagic);
 
-    // ---- quantize and store ----------------------------------------------------
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int u = gi * 4 * C::kTPG + j * C::kTPG + li;
+      const int u = in_unit_grouped<G>(gi, li, j);
       if (u >= units) continue;
-      int uo;
-      if (G <= 16) uo = u;
-      else if (G == 64) uo = gi * 4 + swap2(j);
-      else if (G == 256) uo = gi * 16 + swap2(j) * 4 + swap2(li);
-      else uo = gi * 64 + swap2(j) * 16 + swap_digit_bits4(li);
-      float qr[16];   // rounded codes as floats (integers), in output order
-      bool near_half = false;
-#pragma unroll
-      for (int p = 0; p < 16; p += 2) {
-        // output sign of the register digits (same function as the input sign)
-        const float z0 = static_sign<G>(j, p) ? -v[j][p] : v[j][p];
-        const float z1 = static_sign<G>(j, p + 1) ? -v[j][p + 1] : v[j][p + 1];
-        const unsigned long long q = mul2(f2pack(z0, z1), rcp2);
-        const unsigned long long t2 = sub2(add2(q, magic2), magic2);
-        const unsigned long long e = sub2(q, t2);
-        float e0, e1, t0, t1;
-        f2unpack(e, e0, e1);
-        f2unpack(t2, t0, t1);
-        near_half |= (fabsf(e0) > kNearHalf) | (fabsf(e1) > kNearHalf);
-        qr[out_pos<G>(p)] = t0;
-        qr[out_pos<G>(p + 1)] = t1;
-      }
-      if (near_half) {
-        // exact IEEE quotient for the values near a rounding boundary
-#pragma unroll
-        for (int p = 0; p < 16; ++p) {
-          const float z = static_sign<G>(j, p) ? -v[j][p] : v[j][p];
-          const float q = z * rcp;
-          const float tt = (q + kMagic) - kMagic;
-          if (fabsf(q - tt) > kNearHalf) qr[out_pos<G>(p)] = rintf(__fdiv_rn(z, d));
-        }
-      }
-      if (zero_row) {
-#pragma unroll
-        for (int p = 0; p < 16; ++p) qr[p] = 0.0f;
-      }
+      const int uo = out_unit<G>(u, gi, li, j);
+      float qr[16];
+      quantize_unit<G>(v[j], j, d, rcp, zero_row, qr);
       if (OUT == kPackI8) {
         int8_t* dst = static_cast<int8_t*>(out_codes) + row * static_cast<int64_t>(K) + 16 * uo;
-        uint32_t b[16];
-#pragma unroll
-        for (int p = 0; p < 16; ++p) b[p] = __float_as_uint(qr[p] + kMagic);  // low byte = code
-        uint4 wv;
-        wv.x = pack4_low_bytes(b[0], b[1], b[2], b[3]);
-        wv.y = pack4_low_bytes(b[4], b[5], b[6], b[7]);
-        wv.z = pack4_low_bytes(b[8], b[9], b[10], b[11]);
-        wv.w = pack4_low_bytes(b[12], b[13], b[14], b[15]);
-        *reinterpret_cast<uint4*>(dst) = wv;
+        *reinterpret_cast<uint4*>(dst) = codes_i8(qr);
       } else {
         __half* dst = static_cast<__half*>(out_codes) + row * static_cast<int64_t>(K) + 16 * uo;
-        uint32_t hw[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          __half2 h = __floats2half2_rn(qr[2 * k], qr[2 * k + 1]);
-          hw[k] = *reinterpret_cast<uint32_t*>(&h);
-        }
-        reinterpret_cast<uint4*>(dst)[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-        reinterpret_cast<uint4*>(dst)[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+        uint4 lo, hi;
+        codes_f16(qr, lo, hi);
+        reinterpret_cast<uint4*>(dst)[0] = lo;
+        reinterpret_cast<uint4*>(dst)[1] = hi;
       }
     }
   }
 }
 
+// ---- pack_tma_kernel: TMA-fed persistent pipeline ----------------------------
+
+constexpr int kTmaMaxStages = 4;
+
+struct PackTmaParams {
+  CUtensorMap tmap;     // X as [M][L][E] elements (E per 128-B line), box {E, Lb, rbox}, 128-B swizzle
+  void* out;            // codes [M, K], int8 or binary16
+  float* scales;        // [M]
+  int64_t M;
+  int64_t nblocks;      // ceil(M / R)
+  int K;
+  int R;                // rows per block
+  int tpr;              // threads per row
+  int L;                // 128-byte lines per row
+  int Lb;               // lines per TMA box
+  int rbox;             // rows per TMA box: R when Lb == L (one box per block), else 1
+  int nstages;
+  uint32_t stage_bytes; // R * L * 128 rounded up to 1024
+  uint32_t out_bytes;   // R * K * code bytes rounded up to 128
+};
+
+// Shared memory (base aligned to 1024 B):
+//   [nstages][stage_bytes]  input blocks, 128-byte swizzled lines
+//   [2][out_bytes]          codes of the two most recent blocks
+//   [kTmaMaxStages] u64     "stage full" barriers
+//   [2][R] u64              tagged row absmax
+//   int                     abort flag
+template <int G, typename TIn, int OUT>
+__global__ void __launch_bounds__(kMaxThreads)
+pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
+  using C = Geo<G>;
+  constexpr int ESZ = static_cast<int>(sizeof(TIn));
+  constexpr int OSZ = (OUT == kPackI8) ? 1 : 2;
+  constexpr int CPU = InTraits<TIn>::kChunksPerUnit;
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
+  uint8_t* in_base = smem;
+  uint8_t* out_base = smem + static_cast<size_t>(p.nstages) * p.stage_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(out_base + 2 * static_cast<size_t>(p.out_bytes));
+  unsigned long long* s_amax = reinterpret_cast<unsigned long long*>(full + kTmaMaxStages);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_amax + 2 * p.R);
+  int* err = &g_pack_error;
+
+  const int tid = threadIdx.x;
+  const int K = p.K;
+  const int R = p.R;
+  const int tpr = p.tpr;
+  const int lr = tid / tpr;
+  const int t = tid - lr * tpr;
+  const int units = K >> 4;
+  const int gi = t / C::kTPG;
+  const int li = t - gi * C::kTPG;
+  const bool in_cta_row = lr < R;
+  const int lr_read = in_cta_row ? lr : 0;  // padding threads read row 0 and store nothing
+  const int S = p.nstages;
+
+  for (int i = tid; i < 2 * R; i += blockDim.x) s_amax[i] = 0ull;
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
+    *abort_flag = 0;
+    fence_mbarrier_init();
+    tma_prefetch_desc(&p.tmap);
+  }
+  __syncthreads();
+
+  const uint64_t pol_in = l2_policy_evict_first();
+  const uint32_t block_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(p.L) * 128u;
+  // Thread 0 only: load block `blk` into stage `stage`.
+  auto issue = [&](int64_t blk, int stage) {
+    uint8_t* dst = in_base + static_cast<size_t>(stage) * p.stage_bytes;
+    const int64_t row0 = blk * R;
+    if (p.Lb == p.L) {  // one box holds the whole block
+      mbar_arrive_expect_tx(&full[stage], block_bytes);  // rows past M are zero-filled and still counted
+      tma_load_3d(dst, &p.tmap, &full[stage], 0, 0, static_cast<int32_t>(row0), pol_in);
+    } else {
+      const int64_t rem = p.M - row0;
+      const int rows = rem < R ? static_cast<int>(rem) : R;
+      mbar_arrive_expect_tx(&full[stage], static_cast<uint32_t>(rows) * p.L * 128u);
+      for (int r = 0; r < rows; ++r)
+        for (int l0 = 0; l0 < p.L; l0 += p.Lb)
+          tma_load_3d(dst + (static_cast<size_t>(r) * p.L + l0) * 128, &p.tmap, &full[stage], 0, l0,
+                      static_cast<int32_t>(row0 + r), pol_in);
+    }
+  };
+
+  const LaneSigns<G> ls = lane_signs<G>(li);
+  const int seg = tpr & -tpr;
+  const int segw = seg < 32 ? seg : 32;
+  // units of this thread: round-robin over the row for G <= 16, the group's top
+  // digit for G >= 64
+  int u_of[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u_of[j] = (G <= 16) ? t + tpr * j : in_unit_grouped<G>(gi, li, j);
+
+  const int64_t stride = gridDim.x;
+  int64_t n_issued = 0;  // thread 0: blocks issued (block i of this CTA goes to stage i % S)
+  if (tid == 0)
+    for (int s = 0; s < S - 1; ++s)
+      if (blockIdx.x + s * stride < p.nblocks) { issue(blockIdx.x + s * stride, s); ++n_issued; }
+
+  int it = 0;
+  bool aborted = false;
+  for (int64_t blk = blockIdx.x; blk < p.nblocks; blk += stride, ++it) {
+    const int stage = it % S;
+    const uint32_t phase = static_cast<uint32_t>((it / S) & 1);
+    if (tid == 0) {
+      const int64_t nb = blk + (S - 1) * stride;
+      if (nb < p.nblocks) { issue(nb, (it + S - 1) % S); ++n_issued; }
+    }
+    const bool landed = mbar_wait(&full[stage], phase, abort_flag, err);
+
+    const int64_t row = blk * R + lr;
+    const bool active = in_cta_row && row < p.M;
+    const uint8_t* sin = in_base + static_cast<size_t>(stage) * p.stage_bytes;
+
+    float v[4][16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int u = u_of[j];
+      uint4 c[CPU];
+      if (u < units) {
+#pragma unroll
+        for (int k = 0; k < CPU; ++k) {
+          // byte offset in the block, then the 128-byte swizzle of TMA
+          const uint32_t o = static_cast<uint32_t>((lr_read * K + 16 * u) * ESZ + 16 * k);
+          const uint32_t line = o >> 7;
+          const uint32_t phys = (line << 7) | ((((o >> 4) & 7u) ^ (line & 7u)) << 4);
+          c[k] = *reinterpret_cast<const uint4*>(sin + phys);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < CPU; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      unit_to_f32<TIn>(c, v[j]);
+    }
+    rotate64<G>(v, ls);
+
+    unsigned abits = __float_as_uint(absmax64(v));
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1)
+      if (off < segw) abits = max(abits, __shfl_xor_sync(0xffffffffu, abits, off));
+    const unsigned long long tag = static_cast<unsigned long long>(it + 1) << 32;
+    const int slot = it & 1;
+    if (active && (t % segw) == 0) atomicMax(&s_amax[slot * R + lr], tag | abits);
+    // the bulk store that last read this block's code buffer (two blocks ago)
+    // must have finished reading it
+    if (tid == 0) bulk_wait_read<1>();
+    if (__syncthreads_or(!landed)) { aborted = true; break; }
+
+    uint8_t* sout = out_base + static_cast<size_t>(it & 1) * p.out_bytes;
+    if (active) {
+      const float amax_z = __uint_as_float(static_cast<unsigned>(s_amax[slot * R + lr] & 0xffffffffull));
+      // X_rot = z * 2^-n exactly, so max |X_rot| = amax_z * 2^-n.
+      const float s = __fdiv_rn(amax_z * C::kInvScale, 127.0f);
+      if (t == 0) p.scales[row] = s;
+      const float d = held_divisor<G>(s, ls.flip);
+      const bool zero_row = (s == 0.0f);
+      const float rcp = zero_row ? 0.0f : __frcp_rn(d);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int u = u_of[j];
+        if (u >= units) continue;
+        const int uo = out_unit<G>(u, gi, li, j);
+        float qr[16];
+        quantize_unit<G>(v[j], j, d, rcp, zero_row, qr);
+        uint8_t* dst = sout + static_cast<size_t>(lr * K + 16 * uo) * OSZ;
+        if (OUT == kPackI8) {
+          *reinterpret_cast<uint4*>(dst) = codes_i8(qr);
+        } else {
+          uint4 lo, hi;
+          codes_f16(qr, lo, hi);
+          reinterpret_cast<uint4*>(dst)[0] = lo;
+          reinterpret_cast<uint4*>(dst)[1] = hi;
+        }
+      }
+    }
+    fence_proxy_async_smem();  // make the codes visible to the bulk copy
+    __syncthreads();
+    if (tid == 0) {
+      const int64_t rem = p.M - blk * R;
+      const int64_t rows = rem < R ? rem : R;
+      uint8_t* gdst = static_cast<uint8_t*>(p.out) + static_cast<size_t>(blk * R) * K * OSZ;
+      bulk_store(gdst, sout, static_cast<uint32_t>(rows * K * OSZ));
+      bulk_commit();
+    }
+  }
+  if (tid == 0) {
+    bulk_wait_all();
+    if (aborted) {
+      // no copy may land after the CTA exits: wait (bounded) for the blocks
+      // that were issued but not consumed
+      for (int64_t i = it; i < n_issued; ++i)
+        mbar_wait(&full[i % S], static_cast<uint32_t>((i / S) & 1), nullptr, err);
+    }
+  }
+}
+
+// ---- launchers ----------------------------------------------------------------
+
 int gcd_int(int a, int b) { while (b) { int t = a % b; a = b; b = t; } return a; }
 
+// Raise a kernel's dynamic shared-memory limit once per device (and size).
+// `configured` is that kernel's own record of the limit set on each device.
+std::mutex g_smem_mu;
+
+template <typename Kern>
+int ensure_smem(Kern kern, size_t smem, size_t (&configured)[64]) {
+  std::mutex& mu = g_smem_mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64 || smem > configured[dev]) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev >= 0 && dev < 64) configured[dev] = smem;
+  }
+  return CONVROT_OK;
+}
+
 template <int G, typename TIn, int OUT>
-int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cudaStream_t stream) {
+int launch_pack_cpasync(const void* X, int64_t M, int K, void* out, float* scales, cudaStream_t stream) {
   const int tpr = (K + 63) / 64;
   int rpc = 32 / gcd_int(tpr, 32);
   int threads = tpr * rpc;
@@ -456,24 +751,115 @@ int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cud
   const int two_stage = (static_cast<size_t>(2) * CH * threads * 16 <= kSmemLimit) ? 1 : 0;
   const size_t smem = static_cast<size_t>(two_stage ? 2 : 1) * CH * threads * 16;
   auto kern = pack_kernel<G, TIn, OUT>;
-  static std::mutex mu;
-  static size_t configured_smem = 0;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (smem > configured_smem) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-      if (e != cudaSuccess) return set_cuda_error(e);
-      configured_smem = smem;
-    }
-  }
+  static size_t configured[64] = {};
+  if (int st = ensure_smem(kern, smem, configured)) return st;
   int per_sm = 0;
   cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
   if (e != cudaSuccess) return set_cuda_error(e);
   if (per_sm < 1) per_sm = 1;
   const int64_t nblocks = (M + rpc - 1) / rpc;
   const int64_t grid = std::min<int64_t>(nblocks, static_cast<int64_t>(per_sm) * device_sm_count());
-  pack_kernel<G, TIn, OUT><<<static_cast<unsigned>(grid), threads, smem, stream>>>(
+  kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(
       static_cast<const TIn*>(X), M, K, tpr, rpc, nblocks, two_stage, out, scales);
+  return check_launch();
+}
+
+constexpr size_t kSmemPerCtaMax = 227 * 1024;
+constexpr size_t kSmemTwoCtas = 113 * 1024;  // two CTAs per SM
+constexpr uint32_t kTargetBlockBytes = 24 * 1024;
+
+// Shape of the TMA path for rows of K elements, or false when it does not apply.
+template <typename TIn, int OUT>
+bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
+  constexpr int ESZ = static_cast<int>(sizeof(TIn));
+  constexpr int OSZ = (OUT == kPackI8) ? 1 : 2;
+  const int64_t row_in = static_cast<int64_t>(K) * ESZ;
+  if (row_in % 128 != 0) return false;
+  const int L = static_cast<int>(row_in / 128);
+  const int tpr = (K + 63) / 64;
+  if (tpr > kMaxThreads) return false;
+  int R, Lb, rbox;
+  if (L <= 256) {
+    R = static_cast<int>(kTargetBlockBytes / row_in);
+    R = std::max(1, std::min(R, std::min(256, kMaxThreads / tpr)));
+    Lb = L;
+    rbox = R;
+  } else {
+    // one row per block in boxes of Lb lines; every box starts on a 1024-byte
+    // boundary of the swizzle pattern
+    if (L % 8 != 0) return false;
+    Lb = 0;
+    for (int d = 256; d >= 8; d -= 8)
+      if (L % d == 0) { Lb = d; break; }
+    if (Lb == 0) return false;
+    R = 1;
+    rbox = 1;
+  }
+  const uint32_t stage_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * L * 128 + 1023) / 1024) * 1024);
+  const uint32_t out_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * K * OSZ + 127) / 128) * 128);
+  const size_t misc = 1024 + kTmaMaxStages * 8 + 2 * static_cast<size_t>(R) * 8 + 16;
+  int S = 0;
+  for (size_t budget : {kSmemTwoCtas, kSmemPerCtaMax}) {
+    const size_t fixed = misc + 2 * static_cast<size_t>(out_bytes);
+    if (budget <= fixed) continue;
+    S = static_cast<int>(std::min<size_t>(kTmaMaxStages, (budget - fixed) / stage_bytes));
+    if (S >= 2) {
+      smem = fixed + static_cast<size_t>(S) * stage_bytes;
+      break;
+    }
+  }
+  if (S < 2) return false;
+  p.K = K;
+  p.R = R;
+  p.tpr = tpr;
+  p.L = L;
+  p.Lb = Lb;
+  p.rbox = rbox;
+  p.nstages = S;
+  p.stage_bytes = stage_bytes;
+  p.out_bytes = out_bytes;
+  threads = ((R * tpr + 31) / 32) * 32;
+  return true;
+}
+
+template <int G, typename TIn, int OUT>
+int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cudaStream_t stream) {
+  PackTmaParams p;
+  memset(&p, 0, sizeof(p));
+  int threads = 0;
+  size_t smem = 0;
+  if (!plan_tma<TIn, OUT>(K, p, threads, smem))
+    return launch_pack_cpasync<G, TIn, OUT>(X, M, K, out, scales, stream);
+
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return set_cuda_error(cudaErrorNotSupported);
+  constexpr int E = 128 / static_cast<int>(sizeof(TIn));
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(E), static_cast<cuuint64_t>(p.L),
+                              static_cast<cuuint64_t>(M)};
+  const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(K) * sizeof(TIn)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(E), static_cast<cuuint32_t>(p.Lb),
+                             static_cast<cuuint32_t>(p.rbox)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      (sizeof(TIn) == 4) ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = enc(&p.tmap, dt, 3, const_cast<void*>(X), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_cuda_error(cudaErrorInvalidValue);
+  p.out = out;
+  p.scales = scales;
+  p.M = M;
+  p.nblocks = (M + p.R - 1) / p.R;
+
+  auto kern = pack_tma_kernel<G, TIn, OUT>;
+  static size_t configured[64] = {};
+  if (int st = ensure_smem(kern, smem, configured)) return st;
+  int per_sm = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (per_sm < 1) return set_cuda_error(cudaErrorInvalidConfiguration);
+  const int64_t grid = std::min<int64_t>(p.nblocks, static_cast<int64_t>(per_sm) * device_sm_count());
+  kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(p);
   return check_launch();
 }
 
@@ -489,7 +875,6 @@ int dispatch_group(const void* X, int64_t M, int K, int G, void* out, float* sca
     default: return CONVROT_ERR_GROUP;
   }
 }
-
 __device__ __forceinline__ uint32_t pack2_f16(int q0, int q1) {
   __half2 h = __halves2half2(__int2half_rn(q0), __int2half_rn(q1));
   return *reinterpret_cast<uint32_t*>(&h);
@@ -527,6 +912,18 @@ int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
   }
   return out_kind == kPackI8 ? dispatch_group<__half, kPackI8>(X, M, k, G, out_codes, scales, stream)
                              : dispatch_group<__half, kPackF16>(X, M, k, G, out_codes, scales, stream);
+}
+
+int read_and_clear_pack_error() {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_pack_error, sizeof(int));
+  if (e != cudaSuccess) return set_cuda_error(e);
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_pack_error, &zero, sizeof(int));
+    if (e != cudaSuccess) return set_cuda_error(e);
+  }
+  return v;
 }
 
 int launch_widen(const int8_t* src, __half* dst, int64_t n, cudaStream_t stream) {

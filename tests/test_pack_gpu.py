@@ -155,3 +155,30 @@ def test_rounding_ties_and_neighbours(ops):
     Qo4, so4 = oracle.pack(X, 4)
     assert_scales(s4, so4)
     assert_codes(Q4, Qo4)
+
+
+@pytest.mark.parametrize("M,K,G", [(37, 1024, 1024), (130, 2048, 64), (5, 12288, 256),
+                                   (3, 96, 16), (9, 16384, 4), (1000, 1280, 256)])
+def test_fp16_input_shapes(ops, M, K, G):
+    """fp16 activations: rows of whole 128-byte lines (streamed by tensor
+    copies, including a partial last block and rows split over several boxes)
+    and a row length that is not (K = 96)."""
+    rng = workloads.rng_for(M * 7 + K + G)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=20.0, dtype="f16")
+    check(ops, X, G)
+
+
+@pytest.mark.parametrize("M,K,G,dtype", [(300, 3072, 256, "f32"), (7, 16384, 1024, "f32"),
+                                         (50, 12288, 256, "f32"), (77, 1280, 64, "f16"),
+                                         (3, 48, 4, "f32")])
+def test_binary16_code_output(ops, M, K, G, dtype):
+    """The pack that feeds the tensor-core GEMM writes the same codes as
+    binary16 integers."""
+    rng = workloads.rng_for(M + K * 3 + G)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0, dtype=dtype)
+    Q16, s = ops.convrot_pack_activations_f16(dev(X), G)
+    Q16, s = host(Q16), host(s)
+    Qo, so = oracle.pack(X, G)
+    assert_scales(s, so)
+    assert np.array_equal(Q16, np.rint(Q16)) and np.abs(Q16).max() <= 127
+    assert_codes(Q16.astype(np.int32), Qo)
