@@ -529,12 +529,12 @@ struct PackTmaParams {
   int rbox;             // rows per TMA box: R when Lb == L (one box per block), else 1
   int nstages;
   uint32_t stage_bytes; // R * L * 128 rounded up to 1024
-  uint32_t out_bytes;   // R * K * code bytes rounded up to 128
 };
 
 // Shared memory (base aligned to 1024 B):
-//   [nstages][stage_bytes]  input blocks, 128-byte swizzled lines
-//   [2][out_bytes]          codes of the two most recent blocks
+//   [nstages][stage_bytes]  input blocks, 128-byte swizzled lines; once a
+//                           block is in registers its codes are written over
+//                           it (natural layout) and bulk-copied out
 //   [kTmaMaxStages] u64     "stage full" barriers
 //   [2][R] u64              tagged row absmax
 //   int                     abort flag
@@ -550,8 +550,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
   uint8_t* in_base = smem;
-  uint8_t* out_base = smem + static_cast<size_t>(p.nstages) * p.stage_bytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(out_base + 2 * static_cast<size_t>(p.out_bytes));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.nstages) * p.stage_bytes);
   unsigned long long* s_amax = reinterpret_cast<unsigned long long*>(full + kTmaMaxStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(s_amax + 2 * p.R);
   int* err = &g_pack_error;
@@ -610,7 +609,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const int64_t stride = gridDim.x;
   int64_t n_issued = 0;  // thread 0: blocks issued (block i of this CTA goes to stage i % S)
   if (tid == 0)
-    for (int s = 0; s < S - 1; ++s)
+    for (int s = 0; s < S; ++s)
       if (blockIdx.x + s * stride < p.nblocks) { issue(blockIdx.x + s * stride, s); ++n_issued; }
 
   int it = 0;
@@ -618,15 +617,11 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   for (int64_t blk = blockIdx.x; blk < p.nblocks; blk += stride, ++it) {
     const int stage = it % S;
     const uint32_t phase = static_cast<uint32_t>((it / S) & 1);
-    if (tid == 0) {
-      const int64_t nb = blk + (S - 1) * stride;
-      if (nb < p.nblocks) { issue(nb, (it + S - 1) % S); ++n_issued; }
-    }
     const bool landed = mbar_wait(&full[stage], phase, abort_flag, err);
 
     const int64_t row = blk * R + lr;
     const bool active = in_cta_row && row < p.M;
-    const uint8_t* sin = in_base + static_cast<size_t>(stage) * p.stage_bytes;
+    uint8_t* sbuf = in_base + static_cast<size_t>(stage) * p.stage_bytes;
 
     float v[4][16];
 #pragma unroll
@@ -640,7 +635,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
           const uint32_t o = static_cast<uint32_t>((lr_read * K + 16 * u) * ESZ + 16 * k);
           const uint32_t line = o >> 7;
           const uint32_t phys = (line << 7) | ((((o >> 4) & 7u) ^ (line & 7u)) << 4);
-          c[k] = *reinterpret_cast<const uint4*>(sin + phys);
+          c[k] = *reinterpret_cast<const uint4*>(sbuf + phys);
         }
       } else {
 #pragma unroll
@@ -657,12 +652,10 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
     const unsigned long long tag = static_cast<unsigned long long>(it + 1) << 32;
     const int slot = it & 1;
     if (active && (t % segw) == 0) atomicMax(&s_amax[slot * R + lr], tag | abits);
-    // the bulk store that last read this block's code buffer (two blocks ago)
-    // must have finished reading it
-    if (tid == 0) bulk_wait_read<1>();
+    // every thread has its inputs in registers past this barrier, so the
+    // codes may overwrite the stage
     if (__syncthreads_or(!landed)) { aborted = true; break; }
 
-    uint8_t* sout = out_base + static_cast<size_t>(it & 1) * p.out_bytes;
     if (active) {
       const float amax_z = __uint_as_float(static_cast<unsigned>(s_amax[slot * R + lr] & 0xffffffffull));
       // X_rot = z * 2^-n exactly, so max |X_rot| = amax_z * 2^-n.
@@ -678,7 +671,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
         const int uo = out_unit<G>(u, gi, li, j);
         float qr[16];
         quantize_unit<G>(v[j], j, d, rcp, zero_row, qr);
-        uint8_t* dst = sout + static_cast<size_t>(lr * K + 16 * uo) * OSZ;
+        uint8_t* dst = sbuf + static_cast<size_t>(lr * K + 16 * uo) * OSZ;
         if (OUT == kPackI8) {
           *reinterpret_cast<uint4*>(dst) = codes_i8(qr);
         } else {
@@ -695,8 +688,16 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
       const int64_t rem = p.M - blk * R;
       const int64_t rows = rem < R ? rem : R;
       uint8_t* gdst = static_cast<uint8_t*>(p.out) + static_cast<size_t>(blk * R) * K * OSZ;
-      bulk_store(gdst, sout, static_cast<uint32_t>(rows * K * OSZ));
+      bulk_store(gdst, sbuf, static_cast<uint32_t>(rows * K * OSZ));
       bulk_commit();
+      // refill this stage with the block S iterations ahead once the store
+      // has read the codes out of it
+      const int64_t nb = blk + S * stride;
+      if (nb < p.nblocks) {
+        bulk_wait_read<0>();
+        issue(nb, stage);
+        ++n_issued;
+      }
     }
   }
   if (tid == 0) {
@@ -765,14 +766,13 @@ int launch_pack_cpasync(const void* X, int64_t M, int K, void* out, float* scale
 }
 
 constexpr size_t kSmemPerCtaMax = 227 * 1024;
-constexpr size_t kSmemTwoCtas = 113 * 1024;  // two CTAs per SM
-constexpr uint32_t kTargetBlockBytes = 24 * 1024;
+constexpr uint32_t kTargetBlockBytes = 24 * 1024;  // input bytes of one block
+constexpr int kStages = 2;                          // blocks in flight per CTA
 
 // Shape of the TMA path for rows of K elements, or false when it does not apply.
 template <typename TIn, int OUT>
 bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
   constexpr int ESZ = static_cast<int>(sizeof(TIn));
-  constexpr int OSZ = (OUT == kPackI8) ? 1 : 2;
   const int64_t row_in = static_cast<int64_t>(K) * ESZ;
   if (row_in % 128 != 0) return false;
   const int L = static_cast<int>(row_in / 128);
@@ -796,19 +796,11 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
     rbox = 1;
   }
   const uint32_t stage_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * L * 128 + 1023) / 1024) * 1024);
-  const uint32_t out_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * K * OSZ + 127) / 128) * 128);
   const size_t misc = 1024 + kTmaMaxStages * 8 + 2 * static_cast<size_t>(R) * 8 + 16;
-  int S = 0;
-  for (size_t budget : {kSmemTwoCtas, kSmemPerCtaMax}) {
-    const size_t fixed = misc + 2 * static_cast<size_t>(out_bytes);
-    if (budget <= fixed) continue;
-    S = static_cast<int>(std::min<size_t>(kTmaMaxStages, (budget - fixed) / stage_bytes));
-    if (S >= 2) {
-      smem = fixed + static_cast<size_t>(S) * stage_bytes;
-      break;
-    }
-  }
-  if (S < 2) return false;
+  int S = kStages;
+  while (S > 1 && misc + static_cast<size_t>(S) * stage_bytes > kSmemPerCtaMax) --S;
+  smem = misc + static_cast<size_t>(S) * stage_bytes;
+  if (smem > kSmemPerCtaMax) return false;
   p.K = K;
   p.R = R;
   p.tpr = tpr;
@@ -817,7 +809,6 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
   p.rbox = rbox;
   p.nstages = S;
   p.stage_bytes = stage_bytes;
-  p.out_bytes = out_bytes;
   threads = ((R * tpr + 31) / 32) * 32;
   return true;
 }
