@@ -18,19 +18,27 @@
 // add it into per-thread int32 registers, so A is bit-exact for any K up to
 // the int32 limit.
 //
-// Kernel shape. One persistent CTA per SM, 10 warps:
+// Kernel shape. Persistent, one CTA per SM, 10 warps:
 //   warps 0-7  epilogue: drain TMEM chunks into int32 registers, reconstruct,
 //              store (each thread owns one output feature o and 128
 //              activation rows of a tile; a warp stores 128 B per row).
-//   warp 8     TMA producer: streams 128x64 weight and 256x64 activation
-//              fp16 tiles (128-byte swizzle) into a 4-stage ring.
-//   warp 9     MMA issuer: one thread issues tcgen05.mma kind::f16,
-//              M=128 (weight rows) x N=256 (activation rows) x K=16, into one
-//              of two 256-column fp32 TMEM buffers that alternate per chunk,
-//              so the epilogue drains one while the other accumulates.
-// Tiles of all linears sharing the input are enumerated activation-tile-major
-// (every weight tile of every linear for one 256-row activation band, then
-// the next band), so the band stays in L2 while the weights stream past it.
+//   warp 8     TMA producer: streams 64-deep K slices of the weight and
+//              activation binary16 codes (128-byte swizzle) into a ring of
+//              shared-memory stages.
+//   warp 9     MMA issuer: one thread issues tcgen05.mma kind::f16 with
+//              N = 256 activation rows and K = 16 into one of two 256-column
+//              fp32 TMEM accumulators that alternate per K-chunk, so the
+//              epilogue drains one while the other accumulates.
+// Two variants, CG = CTAs per MMA:
+//   CG = 2 (default): CTA pairs (clusters of two). A tile is 256 weight rows x
+//     256 activation rows; each CTA loads 128 rows of each operand per stage
+//     (32 KB, 6 stages) and holds the accumulator of its 128 weight rows. The
+//     even CTA issues the pair's MMAs (M = 256) once both halves have landed on
+//     its "full" barrier; commits arrive on both CTAs' barriers.
+//   CG = 1: single CTAs, 128 weight rows x 256 activation rows per tile
+//     (48 KB, 4 stages); used where clusters cannot be launched.
+// Tiles of all linears sharing the input form one launch, walked in groups of
+// eight activation bands so weight tiles are reused from L2.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -43,15 +51,11 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int BM = 128;               // weight rows per tile (MMA M)
 constexpr int BN = 256;               // activation rows per tile (MMA N)
 constexpr int BK = 64;                // K per pipeline stage: 64 fp16 = 128 B
-constexpr int STAGES = 4;
 constexpr int KB_PER_CHUNK = 16;      // 16 x 64 = 1024 products per exact chunk
 constexpr int UMMA_K = 16;            // K of one kind::f16 MMA
-constexpr int W_TILE_BYTES = BM * BK * 2;
-constexpr int X_TILE_BYTES = BN * BK * 2;
-constexpr int STAGE_BYTES = W_TILE_BYTES + X_TILE_BYTES;
+constexpr int CTA_M = 128;            // weight rows per CTA (its TMEM lanes)
 constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = NUM_EPI_WARPS;
 constexpr int MMA_WARP = NUM_EPI_WARPS + 1;
@@ -59,34 +63,44 @@ constexpr int THREADS = (NUM_EPI_WARPS + 2) * 32;
 constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
 constexpr int MAX_LIN = CONVROT_MAX_LINEARS;
 constexpr int COLS_PER_THREAD = BN / 2;   // two epilogue warpgroups split the columns
-constexpr uint32_t IDESC = idesc_f16_f32(BM, BN);
 constexpr int RASTER_BANDS = 8;       // activation bands per raster group
 
 static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
 
-// shared-memory layout (after aligning the base to 1024 B)
-constexpr int SMEM_STAGES = STAGES * STAGE_BYTES;
-constexpr int SMEM_BARS = SMEM_STAGES;                         // full[S], empty[S], tfull[2], tempty[2], drain
-constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
-constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;            // tmem base (u32), abort flag (int)
-constexpr int SMEM_TOTAL = SMEM_MISC + 16;
-constexpr int SMEM_ALLOC = SMEM_TOTAL + 1024;                  // slack for the 1024-B alignment
+template <int CG>
+struct Geom {
+  static constexpr int TILE_M = CTA_M * CG;           // weight rows per tile (MMA M)
+  static constexpr int X_ROWS = BN / CG;              // activation rows each CTA loads
+  static constexpr int W_BYTES = CTA_M * BK * 2;
+  static constexpr int X_BYTES = X_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
+  static constexpr int STAGES = (CG == 1) ? 4 : 6;
+  static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN);
+  // shared-memory layout (after aligning the base to 1024 B)
+  static constexpr int SMEM_BARS = STAGES * STAGE_BYTES;  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
+  static constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;  // tmem base (u32), abort flag (int)
+  // slack for the 1024-B alignment, and (pairs) one more half tile so that
+  // every operand read of the last stage stays inside the allocation
+  static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024 + (CG == 2 ? X_BYTES : 0);
+};
+static_assert(Geom<1>::SMEM_ALLOC <= 227 * 1024 && Geom<2>::SMEM_ALLOC <= 227 * 1024, "shared memory");
 
 struct GemmParams {
-  CUtensorMap tmap_x;              // activation codes, fp16 [M, K]
-  CUtensorMap tmap_w[MAX_LIN];     // weight codes, fp16 [N_j, K]
+  CUtensorMap tmap_x;              // activation codes, fp16 [M, K], box X_ROWS x 64
+  CUtensorMap tmap_w[MAX_LIN];     // weight codes, fp16 [N_j, K], box 128 x 64
   const float* s_w[MAX_LIN];
   const float* bias[MAX_LIN];
   void* out[MAX_LIN];              // fp32 Y_j or int32 A_j, [M, N_j]
   int N[MAX_LIN];
-  int wtile_start[MAX_LIN + 1];    // prefix sums of weight tiles per linear
+  int wtile_start[MAX_LIN + 1];    // prefix sums of weight tiles (TILE_M rows) per linear
   const float* s_x;
   int M;
   int K;
   int num_kb;                      // ceil(K / BK)
   int n_xtiles;                    // ceil(M / BN)
-  int n_wtiles;                    // sum over linears of ceil(N_j / BM)
+  int n_wtiles;                    // sum over linears of ceil(N_j / TILE_M)
   int total_tiles;
   int n_lin;
   int raw_s32;
@@ -98,9 +112,9 @@ struct TileCoord {
 
 // Raster order: tiles are taken in groups of RASTER_BANDS activation bands;
 // inside a group, consecutive tiles walk the bands of one weight tile before
-// moving to the next weight tile (of the same or the next linear). The ~152
-// tiles in flight then cover ~RASTER_BANDS bands x ~152/RASTER_BANDS weight
-// tiles, which stay in L2 while the group is swept.
+// moving to the next weight tile (of the same or the next linear). The tiles
+// in flight then cover ~RASTER_BANDS bands and a few dozen weight tiles,
+// which stay in L2 while the group is swept.
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   const int per_group = RASTER_BANDS * p.n_wtiles;
   const int g = t / per_group;
@@ -117,24 +131,32 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   return c;
 }
 
+template <int CG>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Gm = Geom<CG>;
+  constexpr int STAGES = Gm::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
 
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BARS);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::SMEM_BARS);
   uint64_t* full = bars;                   // [STAGES]
   uint64_t* empty = bars + STAGES;         // [STAGES]
   uint64_t* tfull = bars + 2 * STAGES;     // [2]
   uint64_t* tempty = bars + 2 * STAGES + 2;
   uint64_t* drain = bars + 2 * STAGES + 4;
-  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + SMEM_MISC);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_MISC + 4);
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + Gm::SMEM_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Gm::SMEM_MISC + 4);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int* err = &g_device_error;
+  // CTA rank in the pair (0 issues the MMAs) and the scheduling unit (a pair or a CTA)
+  const uint32_t rank = (CG == 2) ? (cluster_ctarank() & 1u) : 0u;
+  const bool leader = (rank == 0);
+  const int unit = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int n_units = (CG == 2) ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
 
   if (threadIdx.x == PRODUCER_WARP * 32) {
     for (int s = 0; s < STAGES; ++s) {
@@ -143,7 +165,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], NUM_EPI_WARPS);
+      mbar_init(&tempty[b], NUM_EPI_WARPS * CG);
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -152,11 +174,16 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     for (int j = 0; j < p.n_lin; ++j) tma_prefetch_desc(&p.tmap_w[j]);
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(tmem_base_smem, TMEM_COLS);
-    tmem_relinquish();
+    if (CG == 2) {
+      tmem_alloc_pair(tmem_base_smem, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_base_smem, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_smem;
 
@@ -166,36 +193,49 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_normal();
       const uint64_t pol_w = l2_policy_evict_normal();
+      // the pair's "full" barriers live in the leader CTA
+      const uint32_t full_leader = (CG == 2) ? mapa_shared(smem_u32(full), 0) : smem_u32(full);
       uint32_t stage = 0, phase = 0;
       uint32_t n_issued = 0;  // stage loads issued so far (stage = n % STAGES)
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < p.total_tiles; t += n_units) {
         const TileCoord c = decode_tile(p, t);
+        const int w_row = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
+        const int x_row = c.xt * BN + static_cast<int>(rank) * Gm::X_ROWS;
         for (int kb = 0; kb < p.num_kb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
-          mbar_arrive_expect_tx(&full[stage], STAGE_BYTES);
-          uint8_t* sw = smem + stage * STAGE_BYTES;
-          uint8_t* sx = sw + W_TILE_BYTES;
-          tma_load_2d(sw, &p.tmap_w[c.lin], &full[stage], kb * BK, c.wt * BM, pol_w);
-          tma_load_2d(sx, &p.tmap_x, &full[stage], kb * BK, c.xt * BN, pol_x);
+          uint8_t* sw = smem + stage * Gm::STAGE_BYTES;
+          uint8_t* sx = sw + Gm::W_BYTES;
+          if (CG == 2) {
+            if (leader) mbar_arrive_expect_tx(&full[stage], CG * Gm::STAGE_BYTES);
+            const uint32_t fb = full_leader + stage * 8u;
+            tma_load_2d_pair(sw, &p.tmap_w[c.lin], fb, kb * BK, w_row, pol_w);
+            tma_load_2d_pair(sx, &p.tmap_x, fb, kb * BK, x_row, pol_x);
+          } else {
+            mbar_arrive_expect_tx(&full[stage], Gm::STAGE_BYTES);
+            tma_load_2d(sw, &p.tmap_w[c.lin], &full[stage], kb * BK, w_row, pol_w);
+            tma_load_2d(sx, &p.tmap_x, &full[stage], kb * BK, x_row, pol_x);
+          }
           ++n_issued;
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
       }
-      // No copy may land after the CTA exits: wait (bounded) for the last
-      // phase of every stage that was ever filled.
-      for (uint32_t s = 0; s < STAGES; ++s)
-        if (n_issued > s) {
-          const uint32_t uses = (n_issued - 1 - s) / STAGES + 1;  // times stage s was filled
-          mbar_wait(&full[s], (uses - 1) & 1u, nullptr, err);
-        }
+      // No copy may land after the CTAs exit: the leader waits (bounded) for
+      // the last phase of every stage that was ever filled (its barriers count
+      // both CTAs' bytes); the pair then meets at the final cluster barrier.
+      if (leader)
+        for (uint32_t s = 0; s < STAGES; ++s)
+          if (n_issued > s) {
+            const uint32_t uses = (n_issued - 1 - s) / STAGES + 1;  // times stage s was filled
+            mbar_wait(&full[s], (uses - 1) & 1u, nullptr, err);
+          }
     }
     __syncwarp();
   } else if (warp == MMA_WARP) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, chunk_iter = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+      for (int t = unit; ok && t < p.total_tiles; t += n_units) {
         for (int ch = 0; ok && ch < num_chunks; ++ch) {
           const uint32_t buf = chunk_iter & 1u;
           const uint32_t use = chunk_iter >> 1;
@@ -207,25 +247,27 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sw = smem_u32(smem + stage * STAGE_BYTES);
+            const uint32_t sw = smem_u32(smem + stage * Gm::STAGE_BYTES);
             const uint64_t a_desc = smem_desc_sw128(sw);
-            const uint64_t b_desc = smem_desc_sw128(sw + W_TILE_BYTES);
+            const uint64_t b_desc = smem_desc_sw128(sw + Gm::W_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
               // advance the start address by k * 32 bytes inside the swizzle row
               const uint64_t koff = static_cast<uint64_t>((k * UMMA_K * 2) >> 4);
-              mma_f16_ss(d_tmem, a_desc + koff, b_desc + koff, IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+              const uint32_t acc = (kb > kb0 || k > 0) ? 1u : 0u;
+              if (CG == 2) mma_f16_ss_pair(d_tmem, a_desc + koff, b_desc + koff, Gm::IDESC, acc);
+              else mma_f16_ss(d_tmem, a_desc + koff, b_desc + koff, Gm::IDESC, acc);
             }
-            mma_commit(&empty[stage]);
+            if (CG == 2) mma_commit_pair(&empty[stage], 0x3); else mma_commit(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
-          mma_commit(&tfull[buf]);
+          if (CG == 2) mma_commit_pair(&tfull[buf], 0x3); else mma_commit(&tfull[buf]);
           ++chunk_iter;
         }
       }
       // all issued MMAs complete before TMEM is released
-      mma_commit(drain);
+      if (CG == 2) mma_commit_pair(drain, 0x1); else mma_commit(drain);
       mbar_wait(drain, 0, nullptr, err);
     }
     __syncwarp();
@@ -235,9 +277,11 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     const int quarter = warp & 3;             // TMEM lanes 32*quarter .. +31
     const int half = warp >> 2;               // activation columns half*128 .. +127
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    // the pair's "accumulator free" barriers live in the leader CTA
+    const uint32_t tempty_leader = (CG == 2) ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     uint32_t chunk_iter = 0;
     bool ok = true;
-    for (int t = blockIdx.x; ok && t < p.total_tiles; t += gridDim.x) {
+    for (int t = unit; ok && t < p.total_tiles; t += n_units) {
       const TileCoord c = decode_tile(p, t);
       int acc[COLS_PER_THREAD];
 #pragma unroll
@@ -257,12 +301,15 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[buf]);
+        if (lane == 0) {
+          if (CG == 2) mbar_arrive_cluster(tempty_leader + buf * 8u);
+          else mbar_arrive(&tempty[buf]);
+        }
         ++chunk_iter;
       }
       if (!ok) break;
       const int N = p.N[c.lin];
-      const int o = c.wt * BM + 32 * quarter + lane;
+      const int o = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
       const int r0 = c.xt * BN + half * COLS_PER_THREAD;
       if (o < N) {
         if (p.raw_s32) {
@@ -295,10 +342,11 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   }
 
   tc_fence_before();
-  __syncthreads();
+  if (CG == 2) cluster_sync(); else __syncthreads();
   if (warp == MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (CG == 2) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -321,6 +369,88 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
   return CONVROT_OK;
 }
 
+template <int CG>
+int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, int64_t K,
+                const GemmLinear* lins, int n_lin, bool raw_s32) {
+  using Gm = Geom<CG>;
+  memset(&p, 0, sizeof(p));
+  int st = make_tmap(&p.tmap_x, x16, M, K, Gm::X_ROWS);
+  if (st) return st;
+  int wt = 0;
+  for (int j = 0; j < n_lin; ++j) {
+    st = make_tmap(&p.tmap_w[j], lins[j].w16, lins[j].N, K, CTA_M);
+    if (st) return st;
+    p.s_w[j] = lins[j].s_w;
+    p.bias[j] = lins[j].bias;
+    p.out[j] = lins[j].out;
+    p.N[j] = static_cast<int>(lins[j].N);
+    p.wtile_start[j] = wt;
+    wt += static_cast<int>((lins[j].N + Gm::TILE_M - 1) / Gm::TILE_M);
+  }
+  p.wtile_start[n_lin] = wt;
+  p.s_x = s_x;
+  p.M = static_cast<int>(M);
+  p.K = static_cast<int>(K);
+  p.num_kb = static_cast<int>((K + BK - 1) / BK);
+  p.n_xtiles = static_cast<int>((M + BN - 1) / BN);
+  p.n_wtiles = wt;
+  const int64_t total = static_cast<int64_t>(p.n_xtiles) * wt;
+  if (total > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  p.total_tiles = static_cast<int>(total);
+  p.n_lin = n_lin;
+  p.raw_s32 = raw_s32 ? 1 : 0;
+  return CONVROT_OK;
+}
+
+// Raise the kernel's shared-memory limit once per device.
+template <int CG>
+int configure_kernel() {
+  static std::mutex mu;
+  static uint64_t configured = 0;  // bit d: attribute set on device d
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev >= 64 || !((configured >> dev) & 1u)) {
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Geom<CG>::SMEM_ALLOC);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    if (dev < 64) configured |= (1ull << dev);
+  }
+  return CONVROT_OK;
+}
+
+// Co-resident CTA pairs on the current device (0 if pairs cannot launch), cached per device.
+int max_pairs() {
+  static std::mutex mu;
+  static int cached[64];
+  static bool known[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!known[dev]) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Geom<2>::SMEM_ALLOC;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2>, &cfg) != cudaSuccess) {
+      cudaGetLastError();  // clear the sticky launch-query error
+      n = 0;
+    }
+    cached[dev] = n;
+    known[dev] = true;
+  }
+  return cached[dev];
+}
+
 }  // namespace
 
 EncodeTiledFn get_encode_fn() {
@@ -340,48 +470,33 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream) {
   if (M == 0) return CONVROT_OK;
   GemmParams p;
-  memset(&p, 0, sizeof(p));
-  int st = make_tmap(&p.tmap_x, x16, M, K, BN);
-  if (st) return st;
-  int wt = 0;
-  for (int j = 0; j < n_lin; ++j) {
-    st = make_tmap(&p.tmap_w[j], lins[j].w16, lins[j].N, K, BM);
-    if (st) return st;
-    p.s_w[j] = lins[j].s_w;
-    p.bias[j] = lins[j].bias;
-    p.out[j] = lins[j].out;
-    p.N[j] = static_cast<int>(lins[j].N);
-    p.wtile_start[j] = wt;
-    wt += static_cast<int>((lins[j].N + BM - 1) / BM);
+  if (int st = configure_kernel<2>()) return st;
+  const int pairs = max_pairs();
+  if (pairs > 0) {
+    if (int st = fill_params<2>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
+    if (p.total_tiles == 0) return CONVROT_OK;
+    const int n = std::min(p.total_tiles, pairs);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * n, 1, 1);
+    cfg.blockDim = dim3(THREADS, 1, 1);
+    cfg.dynamicSmemBytes = Geom<2>::SMEM_ALLOC;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2>, p);
+    if (e != cudaSuccess) return set_cuda_error(e);
+    return check_launch();
   }
-  p.wtile_start[n_lin] = wt;
-  p.s_x = s_x;
-  p.M = static_cast<int>(M);
-  p.K = static_cast<int>(K);
-  p.num_kb = static_cast<int>((K + BK - 1) / BK);
-  p.n_xtiles = static_cast<int>((M + BN - 1) / BN);
-  p.n_wtiles = wt;
-  const int64_t total = static_cast<int64_t>(p.n_xtiles) * wt;
-  if (total == 0) return CONVROT_OK;
-  if (total > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
-  p.total_tiles = static_cast<int>(total);
-  p.n_lin = n_lin;
-  p.raw_s32 = raw_s32 ? 1 : 0;
-
-  static std::mutex mu;
-  static uint64_t configured = 0;  // bit d: attribute set on device d
-  int dev = 0;
-  cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 64 || !((configured >> dev) & 1u)) {
-      cudaError_t e = cudaFuncSetAttribute(convrot_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_ALLOC);
-      if (e != cudaSuccess) return set_cuda_error(e);
-      if (dev < 64) configured |= (1ull << dev);
-    }
-  }
-  const int grid = static_cast<int>(std::min<int64_t>(total, device_sm_count()));
-  convrot_gemm_kernel<<<grid, THREADS, SMEM_ALLOC, stream>>>(p);
+  if (int st = configure_kernel<1>()) return st;
+  if (int st = fill_params<1>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
+  if (p.total_tiles == 0) return CONVROT_OK;
+  const int grid = std::min(p.total_tiles, device_sm_count());
+  convrot_gemm_kernel<1><<<grid, THREADS, Geom<1>::SMEM_ALLOC, stream>>>(p);
   return check_launch();
 }
 
