@@ -310,31 +310,40 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       if (!ok) break;
       const int N = p.N[c.lin];
       const int o = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
+      const bool o_ok = o < N;
       const int r0 = c.xt * BN + half * COLS_PER_THREAD;
-      if (o < N) {
-        if (p.raw_s32) {
+      if (p.raw_s32) {
+        if (o_ok) {
           int32_t* A = static_cast<int32_t*>(p.out[c.lin]);
 #pragma unroll
           for (int i = 0; i < COLS_PER_THREAD; ++i) {
             const int r = r0 + i;
             if (r < p.M) st_global_hint(A + static_cast<int64_t>(r) * N + o, acc[i], pol_y);
           }
-        } else {
-          float* Y = static_cast<float*>(p.out[c.lin]);
-          const float* sw_ptr = p.s_w[c.lin];
-          const float* b_ptr = p.bias[c.lin];
-          const float sw = sw_ptr ? __ldg(sw_ptr + o) : 1.0f;
-          const float bb = b_ptr ? __ldg(b_ptr + o) : 0.0f;
+        }
+      } else {
+        // the warp's 128 row scales: four per lane, broadcast by shuffles
+        float sxv[COLS_PER_THREAD / 32];
 #pragma unroll
-          for (int i = 0; i < COLS_PER_THREAD; ++i) {
-            const int r = r0 + i;
-            if (r < p.M) {
-              // float(A) * s_x * s_w + b, one rounding per operation, in that order
-              float y = __fmul_rn(__int2float_rn(acc[i]), __ldg(p.s_x + r));
-              if (sw_ptr) y = __fmul_rn(y, sw);
-              if (b_ptr) y = __fadd_rn(y, bb);
-              st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
-            }
+        for (int k = 0; k < COLS_PER_THREAD / 32; ++k) {
+          const int r = r0 + 32 * k + lane;
+          sxv[k] = (r < p.M) ? __ldg(p.s_x + r) : 0.0f;
+        }
+        float* Y = static_cast<float*>(p.out[c.lin]);
+        const float* sw_ptr = p.s_w[c.lin];
+        const float* b_ptr = p.bias[c.lin];
+        const float sw = (o_ok && sw_ptr) ? __ldg(sw_ptr + o) : 1.0f;
+        const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < COLS_PER_THREAD; ++i) {
+          const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
+          const int r = r0 + i;
+          if (o_ok && r < p.M) {
+            // float(A) * s_x * s_w + b, one rounding per operation, in that order
+            float y = __fmul_rn(__int2float_rn(acc[i]), sx);
+            if (sw_ptr) y = __fmul_rn(y, sw);
+            if (b_ptr) y = __fadd_rn(y, bb);
+            st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
           }
         }
       }
