@@ -165,7 +165,7 @@ class ClockSampler:
 def gemm_traffic(kernel_src_hash):
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was
     taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemm_dit_qkv_traffic.json")
+    p = os.path.join(ROOT, "profiles", "gemm_dit_qkv_traffic.json")  # written from an ncu capture
     try:
         with open(p) as f:
             d = json.load(f)
@@ -276,22 +276,23 @@ def run_gpu(args, rank, world, local_rank):
         "traffic": gemm_traffic(source_hash()),
     }
 
-    # ---- e2e: one convrot_linear call with host buffers -------------------
+    # ---- e2e: one convrot_linear_host call with host buffers ----------------
+    # X and the outputs in pinned host memory; the library copies row chunks
+    # in and out on two copy streams while it packs and multiplies.
     X_host = torch.from_numpy(case.X).pin_memory()
     Y_host = [torch.empty((w.M, n), dtype=torch.float32).pin_memory() for n in w.Ns]
-    Xd = torch.empty_like(X)
-    ws = torch.empty((ops.convrot_linear_workspace_size(w.M, w.K),), dtype=torch.uint8, device=dev)
-    wdesc2 = ops.make_weights(q16s, scales, biases, Ys)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    n_total = sum(w.Ns)
+    ws = torch.empty((ops.convrot_linear_host_workspace_size(w.M, w.K, ops.F32, n_total, 0),),
+                     dtype=torch.uint8, device=dev)
+    wdesc2 = ops.make_weights(q16s, scales, biases, Y_host)
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():
-        Xd.copy_(X_host, non_blocking=True)
-        st = L.convrot_linear(Xd.data_ptr(), ops.F32, w.M, w.K, w.G, wdesc2, len(q16s),
-                              ws.data_ptr(), ws.numel(), sp)
+        st = L.convrot_linear_host(X_host.data_ptr(), ops.F32, w.M, w.K, w.G, wdesc2, len(q16s), 0,
+                                   ws.data_ptr(), ws.numel(), sp, s_in.cuda_stream, s_out.cuda_stream)
         if st:
-            raise ops.ConvrotError(st, "convrot_linear")
-        for yh, yd in zip(Y_host, Ys):
-            yh.copy_(yd, non_blocking=True)
+            raise ops.ConvrotError(st, "convrot_linear_host")
 
     for _ in range(2):
         e2e_step()
@@ -310,11 +311,12 @@ def run_gpu(args, rank, world, local_rank):
     e2e = {"value": world * ops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
            "h2d_bytes_per_step": int(X_host.numel() * 4),
            "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in Y_host)),
-           "ms_per_step": e2e_ms, "api": "convrot_linear (one call) + pinned H2D/D2H copies"}
+           "ms_per_step": e2e_ms,
+           "api": "convrot_linear_host (one call; pinned host X and Y, chunked copies overlapped with compute)"}
     # check parity of the e2e output against the timed path's output
-    Yt = [y.clone() for y in Ys]
     step(); gemm()
     torch.cuda.synchronize()
+    Yt = [y.cpu() for y in Ys]
 
     # ---- pack-only sweep (X fp32 [4096, 3072], every G) -------------------
     pw = workloads.get("pack_sweep")
@@ -343,13 +345,42 @@ def run_gpu(args, rank, world, local_rank):
         ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
         gbs = pack_bytes / (ms * 1e-3) / 1e9
         sweep[str(G)] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    # long rows: the MLP pair's repack input, X fp32 [4608, 12288] -> binary16 codes
+    ML, KL = 4608, 12288
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(4)
+    Xl = torch.randn((ML, KL), generator=gen, device=dev)
+    Ql = torch.empty((ML, KL), dtype=torch.float16, device=dev)
+    sl = torch.empty((ML,), dtype=torch.float32, device=dev)
+    large_bytes = ML * KL * 4 + ML * KL * 2 + ML * 4
+    for _ in range(3):
+        L.convrot_pack_activations_f16(Xl.data_ptr(), ops.F32, ML, KL, 256, Ql.data_ptr(), sl.data_ptr(), sp)
+    times = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        st = L.convrot_pack_activations_f16(Xl.data_ptr(), ops.F32, ML, KL, 256, Ql.data_ptr(), sl.data_ptr(), sp)
+        b.record(stream)
+        if st:
+            raise ops.ConvrotError(st, "pack long rows")
+        times.append((a, b))
+    torch.cuda.synchronize()
+    ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
+    gbs = large_bytes / (ms * 1e-3) / 1e9
+    large = {"workload": f"X fp32 [{ML},{KL}] ~N(0,1) seed 4, G=256 -> binary16 codes + s",
+             "bytes": large_bytes, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    del Xl, Ql, sl
+
     pack = {
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
         "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
         "peak_kind": f"{peak_kind} HBM copy", "by_group": sweep,
         "fused_step_pack": {"us": round(float(pack_ms.mean()) * 1e3, 2),
                             "bytes": fused_pack_bytes,
-                            "GB/s": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9, 1)},
+                            "GB/s": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9, 1),
+                            "frac": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9 / hbm, 4)},
+        "long_rows": large,
     }
 
     result = {
@@ -362,7 +393,7 @@ def run_gpu(args, rank, world, local_rank):
         "clocks": clocks,
         "timing": {"step_ms_median": float(np.median(step_ms)), "pack_us_mean": float(pack_ms.mean() * 1e3),
                    "gemm_us_mean": float(gemm_ms.mean() * 1e3), "wall_s_timed_loop": wall},
-        "e2e_parity_max_abs_diff": float(max((a - b).abs().max().item() for a, b in zip(Yt, Ys))),
+        "e2e_parity_max_abs_diff": float(max((a - b).abs().max().item() for a, b in zip(Yt, Y_host))),
     }
     return result, case, w
 

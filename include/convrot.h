@@ -208,6 +208,38 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
                           const convrot_weight* weights, int n_weights, void* stream);
 
+/*
+ * convrot_linear_host_workspace_size -- device bytes convrot_linear_host needs:
+ * two sets of chunk buffers (input rows, binary16 codes, row scales and the
+ * output rows of all linears, n_total = sum of their N). chunk_rows = 0 picks
+ * the library default (768 rows). Returns 0 for invalid arguments.
+ */
+size_t convrot_linear_host_workspace_size(int64_t M, int64_t K, int x_dtype,
+                                          int64_t n_total, int64_t chunk_rows);
+
+/*
+ * convrot_linear_host -- convrot_linear with X and every Y_j in HOST memory
+ * (the weights, scales and biases stay in device memory). The rows are
+ * processed in chunks of chunk_rows: each chunk is copied in on
+ * copy_in_stream, packed and multiplied on `stream`, and its output rows
+ * copied out on copy_out_stream, so transfers overlap compute. Host arrays
+ * should be pinned (page-locked) for the transfers to overlap.
+ *   X_host     [M,K] fp32/fp16 host array.
+ *   weights    as convrot_linear; every Y is a host array [M,N_j] fp32.
+ *   chunk_rows rows per chunk (0 = default 768; multiples of 256 suit the GEMM).
+ *   workspace  device scratch, >= convrot_linear_host_workspace_size(...).
+ *   stream, copy_in_stream, copy_out_stream: cudaStream_t (NULL copy streams
+ *              mean `stream`: correct but without overlap). The call is
+ *              ordered after earlier work on `stream`, and later work on
+ *              `stream` runs after every output copy has completed.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_WORKSPACE,
+ *         ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, int G,
+                        const convrot_weight* weights, int n_weights, int64_t chunk_rows,
+                        void* workspace, size_t workspace_bytes, void* stream,
+                        void* copy_in_stream, void* copy_out_stream);
+
 /* Size of the fixed device array that convrot_linear_noalloc uses (32 MiB). */
 #define CONVROT_NOALLOC_SCRATCH_BYTES (32u << 20)
 

@@ -72,6 +72,9 @@ SIGNATURES = {
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
     "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
+    "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
+    "convrot_linear_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I64, _VP, _SZ,
+                                 _VP, _VP, _VP]),
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_device_status": (_I, [_VP]),
 }
@@ -269,6 +272,39 @@ def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, 
         weights = make_weights(q16s, scales, biases, Ys)
     _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _stream(stream)),
            "convrot_linear_packed")
+    return Ys
+
+
+def convrot_linear_host_workspace_size(M: int, K: int, x_dtype: int, n_total: int, chunk_rows: int = 0) -> int:
+    return int(lib().convrot_linear_host_workspace_size(M, K, x_dtype, n_total, chunk_rows))
+
+
+def convrot_linear_host(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
+                        scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
+                        Ys: Optional[List[torch.Tensor]] = None, chunk_rows: int = 0, workspace=None,
+                        stream=None, copy_in_stream=None, copy_out_stream=None, weights=None
+                        ) -> List[torch.Tensor]:
+    """convrot_linear on host arrays: X [M,K] and the outputs live in (pinned)
+    host memory, the weights on the device; transfers of row chunks overlap
+    compute on the given copy streams."""
+    xd = _xdtype(X)
+    if X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous host tensor")
+    M, K = X.shape
+    dev = q16s[0].device
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, pin_memory=True) for q in q16s]
+    for y in Ys:
+        if y.is_cuda or y.dtype != torch.float32 or not y.is_contiguous():
+            raise ValueError("every Y must be a contiguous float32 host tensor")
+    n_total = sum(q.shape[0] for q in q16s)
+    ws = _workspace(convrot_linear_host_workspace_size(M, K, xd, n_total, chunk_rows), dev, workspace)
+    if weights is None:
+        weights = make_weights(q16s, scales, biases, Ys)
+    _check(lib().convrot_linear_host(X.data_ptr(), xd, M, K, G, weights, len(q16s), chunk_rows, _ptr(ws),
+                                     ws.numel(), _stream(stream), _stream(copy_in_stream) if copy_in_stream else None,
+                                     _stream(copy_out_stream) if copy_out_stream else None),
+           "convrot_linear_host")
     return Ys
 
 

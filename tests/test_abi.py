@@ -120,3 +120,21 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(ops, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         ops.lib()
+
+
+def test_host_pipeline_checks(L):
+    from int8_hadamard_rotated_gb300 import ops
+    ws = L.convrot_linear_host_workspace_size
+    # two sets of (input rows, binary16 codes, scales, outputs), each rounded to 256 bytes
+    r = 768
+    one = (r * 3072 * 4) + (r * 3072 * 2) + ((r * 4 + 255) // 256 * 256) + (r * 9216 * 4)
+    assert ws(4608, 3072, ops.F32, 9216, 0) == 2 * one
+    assert ws(100, 3072, ops.F32, 9216, 0) == ws(100, 3072, ops.F32, 9216, 100)  # chunk clipped to M
+    assert ws(0, 3072, ops.F32, 9216, 0) == 0 and ws(10, 3072, 5, 9216, 0) == 0
+    W = ops.convrot_weight
+    wts = (W * 1)(W(A1, None, None, 64, A2))
+    g = L.convrot_linear_host
+    assert g(A0, ops.F32, 16, 256, 128, wts, 1, 0, A3, 1 << 40, None, None, None) == ops.ERR_GROUP
+    assert g(A0, ops.F32, 16, 256, 256, wts, 1, 0, None, 0, None, None, None) == ops.ERR_WORKSPACE
+    assert g(A0, ops.F32, 16, 256, 256, wts, 1, -1, A3, 1 << 40, None, None, None) == ops.ERR_ARG
+    assert g(A0, ops.F32, 0, 256, 256, wts, 1, 0, None, 0, None, None, None) == ops.OK

@@ -137,3 +137,30 @@ def test_packed_entry_points_match_fused_call(ops):
     # and the packed GEMM equals int8_linear on the int8 codes
     Yc = ops.int8_linear(Q8, s8, Q_w16=Qw16, s_w=s_w, bias=b)
     np.testing.assert_array_equal(host(Yc), host(Ya))
+
+
+@pytest.mark.parametrize("M,K,Ns,G,xd,chunk,streams", [
+    (1000, 1280, (1280,), 256, "f16", 256, True),       # ragged last chunk
+    (4608, 3072, (3072, 3072, 3072), 256, "f32", 0, True),  # the DiT projections, default chunks
+    (300, 512, (256, 96), 64, "f32", 1024, True),        # one chunk larger than M
+    (513, 256, (128,), 4, "f32", 128, False),           # no copy streams: serialized
+])
+def test_host_pipeline_matches_device_call(ops, M, K, Ns, G, xd, chunk, streams):
+    """convrot_linear_host (host X and Y, chunked, overlapped transfers) gives
+    exactly convrot_linear's outputs."""
+    rng = workloads.rng_for(M + K + sum(Ns))
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0, dtype=xd)
+    Ws = [workloads.weights(rng, n, K) for n in Ns]
+    bs = [workloads.biases(rng, n) for n in Ns]
+    preps = [ops.convrot_prepare_weight(dev(W), G) for W in Ws]
+    q16s, scales, biases = [p[2] for p in preps], [p[1] for p in preps], [dev(b) for b in bs]
+    Y_ref = [host(y) for y in ops.convrot_linear(dev(X), G, q16s, scales, biases)]
+    Xh = torch.from_numpy(X).pin_memory()
+    kw = {}
+    if streams:
+        kw = dict(copy_in_stream=torch.cuda.Stream(), copy_out_stream=torch.cuda.Stream())
+    Ys = ops.convrot_linear_host(Xh, G, q16s, scales, biases, chunk_rows=chunk, **kw)
+    torch.cuda.current_stream().synchronize()
+    assert ops.convrot_device_status() == ops.OK
+    for y, r in zip(Ys, Y_ref):
+        np.testing.assert_array_equal(y.numpy(), r)
