@@ -164,13 +164,15 @@ class ClockSampler:
 
 def gemm_traffic(kernel_src_hash):
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was
-    taken on the current kernel source."""
-    p = os.path.join(ROOT, "profiles", "gemm_dit_qkv_traffic.json")  # written from an ncu capture
+    taken on the current kernel source (its `traffic_json:` line)."""
+    p = os.path.join(ROOT, "profiles", "gemm_dit_qkv.md")
     try:
         with open(p) as f:
-            d = json.load(f)
-        if d.get("gemm_cu_sha256") == kernel_src_hash:
-            return d.get("dram_bytes_per_launch")
+            for line in f:
+                if line.startswith("traffic_json:"):
+                    d = json.loads(line.split(":", 1)[1])
+                    if d.get("gemm_cu_sha256") == kernel_src_hash:
+                        return d.get("dram_bytes_per_launch")
     except Exception:
         pass
     return None
