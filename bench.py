@@ -198,16 +198,17 @@ def run_gpu(args, rank, world, local_rank):
 
     # resident inputs and offline weight preparation (untimed)
     X = torch.from_numpy(case.X).to(dev)
-    q16s, scales, biases = [], [], []
+    q16s, scales, biases, plans = [], [], [], []
     for W, b in zip(case.Ws, case.bs):
-        _, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), w.G)
+        q8, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), w.G)
         q16s.append(q16)
         scales.append(s_w)
         biases.append(torch.from_numpy(b).to(dev))
+        plans.append(ops.convrot_weight_chunks(q8))   # exact-chunk plan, also offline
     Ys = [torch.empty((w.M, n), dtype=torch.float32, device=dev) for n in w.Ns]
     Qx16 = torch.empty((w.M, w.K), dtype=torch.float16, device=dev)
     s_x = torch.empty((w.M,), dtype=torch.float32, device=dev)
-    wdesc = ops.make_weights(q16s, scales, biases, Ys)
+    wdesc = ops.make_weights(q16s, scales, biases, Ys, plans)
     L = ops.lib()
     sp = stream.cuda_stream
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
@@ -287,7 +288,7 @@ def run_gpu(args, rank, world, local_rank):
     n_total = sum(w.Ns)
     ws = torch.empty((ops.convrot_linear_host_workspace_size(w.M, w.K, ops.F32, n_total, 0),),
                      dtype=torch.uint8, device=dev)
-    wdesc2 = ops.make_weights(q16s, scales, biases, Y_host)
+    wdesc2 = ops.make_weights(q16s, scales, biases, Y_host, plans)
     e2e_steps = max(3, min(args.steps, 20))
 
     def e2e_step():

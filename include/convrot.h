@@ -155,7 +155,29 @@ typedef struct convrot_weight {
   const float* bias;   /* [N], or NULL (no bias) */
   int64_t N;           /* output features */
   float* Y;            /* [M,N] fp32 output */
+  const int32_t* kchunk; /* [ceil(N/128)] exact-chunk plan from convrot_weight_chunks,
+                            or NULL (chunks of 1024 products) */
 } convrot_weight;
+
+/* Weight rows per entry of a chunk plan. */
+#define CONVROT_CHUNK_ROWS 128
+
+/*
+ * convrot_weight_chunks -- offline exact-chunk plan of a weight for the GEMM.
+ * The tensor-core GEMM accumulates runs of K-products in fp32 and adds the
+ * runs in int32; a run is exact when every partial sum stays below 2^24.
+ * Since every activation code has |q_x| <= 127, a run over the K range R is
+ * exact for output row o whenever 127 * sum_{k in R} |Q_w[o,k]| < 2^24. For
+ * every block of CONVROT_CHUNK_ROWS weight rows this writes the longest run
+ * length L (in units of 64 K-elements; runs start at multiples of L) among
+ * {16, 32, 64, ...} and "all of K" that satisfies that bound for every row of
+ * the block and every run; L = 16 (1024 products) always does.
+ *   Q_w     [N,K] int8 weight codes (convrot_prepare_weight).
+ *   kchunk  [ceil(N/128)] int32 (output).
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS, ERR_CUDA.
+ */
+int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk,
+                          void* stream);
 
 /* Device bytes convrot_linear needs for the shared packed activation. */
 size_t convrot_linear_workspace_size(int64_t M, int64_t K);
@@ -178,12 +200,13 @@ int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
 /*
  * int8_gemm_s32 -- the raw int32 product A = Q_x Q_w^T (no scales), through
  * the same tensor-core GEMM as int8_linear. For exactness checks.
- *   Arguments as int8_linear; A [M,N] int32 (output).
+ *   Arguments as int8_linear; kchunk: the weight's exact-chunk plan
+ *   (convrot_weight_chunks) or NULL; A [M,N] int32 (output).
  * Errors: as int8_linear.
  */
 int int8_gemm_s32(const int8_t* Q_x, int64_t M, int64_t K,
-                  const int8_t* Q_w, const uint16_t* Q_w16, int64_t N,
-                  int32_t* A, void* workspace, size_t workspace_bytes,
+                  const int8_t* Q_w, const uint16_t* Q_w16, const int32_t* kchunk,
+                  int64_t N, int32_t* A, void* workspace, size_t workspace_bytes,
                   void* stream);
 
 /*

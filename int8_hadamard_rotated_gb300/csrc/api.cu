@@ -154,8 +154,8 @@ namespace {
 
 // Shared checks and workspace carving of int8_linear / int8_gemm_s32.
 int int8_gemm_common(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
-                     const int8_t* Q_w, const uint16_t* Q_w16, const float* s_w, const float* bias,
-                     int64_t N, void* out, size_t out_esz, bool raw,
+                     const int8_t* Q_w, const uint16_t* Q_w16, const int32_t* kchunk, const float* s_w,
+                     const float* bias, int64_t N, void* out, size_t out_esz, bool raw,
                      void* workspace, size_t workspace_bytes, void* stream) {
   if (M < 0 || N < 0 || K <= 0) return CONVROT_ERR_ARG;
   if (M == 0 || N == 0) return CONVROT_OK;
@@ -163,7 +163,8 @@ int int8_gemm_common(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
   if (M > 0x7fffffff || N > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
   if (K % 16 != 0 || !aligned16(Q_x) || !aligned16(out) || (s_x && !aligned16(s_x)) ||
       (Q_w && !aligned16(Q_w)) || (Q_w16 && !aligned16(Q_w16)) || (s_w && !aligned16(s_w)) ||
-      (bias && !aligned16(bias)) || (workspace && !aligned16(workspace)))
+      (bias && !aligned16(bias)) || (workspace && !aligned16(workspace)) ||
+      (reinterpret_cast<uintptr_t>(kchunk) & 3u))
     return CONVROT_ERR_ALIGN;
   if (K > CONVROT_MAX_K) return CONVROT_ERR_OVERFLOW;
   const size_t need = int8_linear_workspace_size(M, N, K, Q_w16 != nullptr);
@@ -191,7 +192,7 @@ int int8_gemm_common(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
     if (st) return st;
     w16 = wtmp;
   }
-  GemmLinear lin{w16, s_w, bias, out, N};
+  GemmLinear lin{w16, s_w, bias, out, N, kchunk};
   return launch_gemm(x16, s_x, M, K, &lin, 1, raw, s);
 }
 
@@ -203,14 +204,14 @@ int int8_linear(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
                 const int8_t* Q_w, const uint16_t* Q_w16, const float* s_w,
                 const float* bias, int64_t N, float* Y,
                 void* workspace, size_t workspace_bytes, void* stream) {
-  return int8_gemm_common(Q_x, s_x, M, K, Q_w, Q_w16, s_w, bias, N, Y, 4, false,
+  return int8_gemm_common(Q_x, s_x, M, K, Q_w, Q_w16, nullptr, s_w, bias, N, Y, 4, false,
                           workspace, workspace_bytes, stream);
 }
 
 int int8_gemm_s32(const int8_t* Q_x, int64_t M, int64_t K,
-                  const int8_t* Q_w, const uint16_t* Q_w16, int64_t N,
+                  const int8_t* Q_w, const uint16_t* Q_w16, const int32_t* kchunk, int64_t N,
                   int32_t* A, void* workspace, size_t workspace_bytes, void* stream) {
-  return int8_gemm_common(Q_x, nullptr, M, K, Q_w, Q_w16, nullptr, nullptr, N, A, 4, true,
+  return int8_gemm_common(Q_x, nullptr, M, K, Q_w, Q_w16, kchunk, nullptr, nullptr, N, A, 4, true,
                           workspace, workspace_bytes, stream);
 }
 
@@ -225,7 +226,8 @@ int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    if (!aligned16(w.q16) || !aligned16(w.Y) || (w.scale && !aligned16(w.scale)) || (w.bias && !aligned16(w.bias)))
+    if (!aligned16(w.q16) || !aligned16(w.Y) || (w.scale && !aligned16(w.scale)) || (w.bias && !aligned16(w.bias)) ||
+        (reinterpret_cast<uintptr_t>(w.kchunk) & 3u))
       return CONVROT_ERR_ALIGN;
   }
   for (int j = 0; j < n_weights; ++j) {
@@ -263,7 +265,7 @@ int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N};
+    lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N, w.kchunk};
   }
   if (n == 0) return CONVROT_OK;
   return launch_gemm(x16, s_x, M, K, lins, n, false, s);
@@ -350,6 +352,19 @@ int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
   int st = launch_pack(X, x_dtype, M, K, G, x16, kPackF16, s_x, s);
   if (st) return st;
   return launch_grouped(x16, s_x, M, K, weights, n_weights, s);
+}
+
+int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, void* stream) {
+  if (N < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (N == 0) return CONVROT_OK;
+  if (!Q_w || !kchunk) return CONVROT_ERR_ARG;
+  if (K % 16 != 0 || !aligned16(Q_w) || (reinterpret_cast<uintptr_t>(kchunk) & 3u)) return CONVROT_ERR_ALIGN;
+  if (K > CONVROT_MAX_K) return CONVROT_ERR_OVERFLOW;
+  if (N > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  const size_t nb = static_cast<size_t>((N + CONVROT_CHUNK_ROWS - 1) / CONVROT_CHUNK_ROWS) * 4;
+  if (overlaps(Q_w, static_cast<size_t>(N) * K, kchunk, nb)) return CONVROT_ERR_ALIAS;
+  if (int st = check_device()) return st;
+  return launch_chunk_plan(Q_w, N, K, kchunk, static_cast<cudaStream_t>(stream));
 }
 
 int convrot_device_status(void* stream) {

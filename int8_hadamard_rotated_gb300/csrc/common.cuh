@@ -372,7 +372,11 @@ struct GemmLinear {
   const float* bias;   // [N] or null
   void* out;           // [M,N] fp32 Y or int32 A
   int64_t N;
+  const int32_t* kchunk;  // [ceil(N/128)] exact-chunk plan (64-wide K blocks per chunk) or null
 };
+
+// Exact-chunk plan of int8 weight codes (see convrot_weight_chunks).
+int launch_chunk_plan(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, cudaStream_t stream);
 
 // out_j = epilogue(x16 . w16_j^T) for every linear j; raw_s32 selects int32 A.
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,

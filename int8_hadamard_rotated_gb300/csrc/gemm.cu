@@ -92,6 +92,7 @@ struct GemmParams {
   CUtensorMap tmap_w[MAX_LIN];     // weight codes, fp16 [N_j, K], box 128 x 64
   const float* s_w[MAX_LIN];
   const float* bias[MAX_LIN];
+  const int32_t* kchunk[MAX_LIN];  // exact-chunk plan per 128 weight rows, or null
   void* out[MAX_LIN];              // fp32 Y_j or int32 A_j, [M, N_j]
   int N[MAX_LIN];
   int wtile_start[MAX_LIN + 1];    // prefix sums of weight tiles (TILE_M rows) per linear
@@ -129,6 +130,22 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   c.lin = j;
   c.wt = w - p.wtile_start[j];
   return c;
+}
+
+// K blocks (of BK) per exact fp32 chunk for a tile: the weight's plan for the
+// tile's 128-row blocks (their minimum), or KB_PER_CHUNK (1024 products,
+// always exact) without a plan.
+template <int CG>
+__device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoord& c) {
+  int L = KB_PER_CHUNK;
+  const int32_t* plan = p.kchunk[c.lin];
+  if (plan) {
+    const int b0 = c.wt * CG;
+    const int nblk = (p.N[c.lin] + CTA_M - 1) / CTA_M;
+    L = __ldg(plan + b0);
+    if (CG == 2 && b0 + 1 < nblk) L = min(L, __ldg(plan + b0 + 1));
+  }
+  return max(1, min(L, p.num_kb));
 }
 
 template <int CG>
@@ -187,8 +204,6 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_smem;
 
-  const int num_chunks = (p.num_kb + KB_PER_CHUNK - 1) / KB_PER_CHUNK;
-
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
       const uint64_t pol_x = l2_policy_evict_normal();
@@ -235,15 +250,20 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, chunk_iter = 0;
       bool ok = true;
+      // the next tile's chunk length is read one tile ahead
+      int L_next = (unit < p.total_tiles) ? tile_chunk_kb<CG>(p, decode_tile(p, unit)) : 1;
       for (int t = unit; ok && t < p.total_tiles; t += n_units) {
+        const int L = L_next;
+        if (t + n_units < p.total_tiles) L_next = tile_chunk_kb<CG>(p, decode_tile(p, t + n_units));
+        const int num_chunks = (p.num_kb + L - 1) / L;
         for (int ch = 0; ok && ch < num_chunks; ++ch) {
           const uint32_t buf = chunk_iter & 1u;
           const uint32_t use = chunk_iter >> 1;
           if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          const int kb0 = ch * KB_PER_CHUNK;
-          const int kb1 = min(kb0 + KB_PER_CHUNK, p.num_kb);
+          const int kb0 = ch * L;
+          const int kb1 = min(kb0 + L, p.num_kb);
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
@@ -283,6 +303,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     bool ok = true;
     for (int t = unit; ok && t < p.total_tiles; t += n_units) {
       const TileCoord c = decode_tile(p, t);
+      const int L = tile_chunk_kb<CG>(p, c);
+      const int num_chunks = (p.num_kb + L - 1) / L;
       int acc[COLS_PER_THREAD];
 #pragma unroll
       for (int i = 0; i < COLS_PER_THREAD; ++i) acc[i] = 0;
@@ -391,6 +413,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
     if (st) return st;
     p.s_w[j] = lins[j].s_w;
     p.bias[j] = lins[j].bias;
+    p.kchunk[j] = lins[j].kchunk;
     p.out[j] = lins[j].out;
     p.N[j] = static_cast<int>(lins[j].N);
     p.wtile_start[j] = wt;
@@ -460,7 +483,69 @@ int max_pairs() {
   return cached[dev];
 }
 
+// ---------------------------------------------------------------------------
+// exact-chunk plan of a weight (offline)
+// ---------------------------------------------------------------------------
+
+constexpr int kPlanMaxCands = 16;
+constexpr long long kExactLimit = (1ll << 24) - 1;  // every integer up to this is exact in fp32
+
+// One thread per weight row, one CTA per block of CONVROT_CHUNK_ROWS rows.
+// Candidates: runs of 16 * 2^j K blocks (shorter than K), then all of K. For
+// each candidate, the largest 127 * sum |Q_w| over any run of any row of the
+// block decides whether the candidate is exact.
+__global__ void __launch_bounds__(CONVROT_CHUNK_ROWS)
+chunk_plan_kernel(const int8_t* __restrict__ Q_w, int N, int K, int32_t* __restrict__ kchunk) {
+  const int num_kb = (K + BK - 1) / BK;
+  int cand[kPlanMaxCands];
+  int nc = 0;
+  for (int L = KB_PER_CHUNK; L < num_kb && nc < kPlanMaxCands - 1; L *= 2) cand[nc++] = L;
+  cand[nc++] = num_kb;
+  int run[kPlanMaxCands], mx[kPlanMaxCands];
+  for (int c = 0; c < nc; ++c) run[c] = mx[c] = 0;
+  const int o = blockIdx.x * CONVROT_CHUNK_ROWS + threadIdx.x;
+  if (o < N) {
+    const int8_t* row = Q_w + static_cast<int64_t>(o) * K;
+    for (int kb = 0; kb < num_kb; ++kb) {
+      int sum = 0;
+      const int e1 = min(K, (kb + 1) * BK);
+      for (int e = kb * BK; e < e1; e += 16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + e);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) sum += abs(static_cast<int>(static_cast<int8_t>((w[i] >> (8 * b)) & 0xffu)));
+      }
+      for (int c = 0; c < nc; ++c) {
+        if (kb % cand[c] == 0) run[c] = 0;
+        run[c] += sum;
+        mx[c] = max(mx[c], run[c]);
+      }
+    }
+  }
+  __shared__ int s_max[kPlanMaxCands];
+  if (threadIdx.x < kPlanMaxCands) s_max[threadIdx.x] = 0;
+  __syncthreads();
+  for (int c = 0; c < nc; ++c) atomicMax(&s_max[c], mx[c]);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int best = min(KB_PER_CHUNK, num_kb);  // 1024 products: always exact
+    for (int c = 0; c < nc; ++c)
+      if (static_cast<long long>(s_max[c]) * 127 <= kExactLimit) best = max(best, cand[c]);
+    kchunk[blockIdx.x] = best;
+  }
+}
+
 }  // namespace
+
+int launch_chunk_plan(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, cudaStream_t stream) {
+  if (N == 0) return CONVROT_OK;
+  const int64_t blocks = (N + CONVROT_CHUNK_ROWS - 1) / CONVROT_CHUNK_ROWS;
+  chunk_plan_kernel<<<static_cast<unsigned>(blocks), CONVROT_CHUNK_ROWS, 0, stream>>>(
+      Q_w, static_cast<int>(N), static_cast<int>(K), kchunk);
+  return check_launch();
+}
 
 EncodeTiledFn get_encode_fn() {
   static EncodeTiledFn fn = nullptr;

@@ -152,7 +152,7 @@ extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, i
     for (int j = 0; j < n_weights; ++j) {
       const convrot_weight& w = weights[j];
       if (w.N == 0) continue;
-      lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, B[b].y + off, w.N};
+      lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, B[b].y + off, w.N, w.kchunk};
       off += static_cast<size_t>(m) * w.N;
     }
     if (n > 0)

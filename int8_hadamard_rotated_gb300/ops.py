@@ -37,6 +37,7 @@ F16 = 1
 MAX_LINEARS = 8
 PACK_MAX_K = 32768
 MAX_K = 133144
+CHUNK_ROWS = 128
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -53,7 +54,7 @@ class ConvrotError(RuntimeError):
 class convrot_weight(ctypes.Structure):
     _fields_ = [("q16", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("N", ctypes.c_int64),
-                ("Y", ctypes.c_void_p)]
+                ("Y", ctypes.c_void_p), ("kchunk", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -69,7 +70,8 @@ SIGNATURES = {
     "int8_linear": (_I, [_VP, _VP, _I64, _I64, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_linear_workspace_size": (_SZ, [_I64, _I64]),
     "convrot_linear": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
-    "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "convrot_weight_chunks": (_I, [_VP, _I64, _I64, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
     "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
@@ -203,8 +205,19 @@ def int8_linear(Q_x, s_x, Q_w=None, Q_w16=None, s_w=None, bias=None, Y=None,
     return Y
 
 
-def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None) -> torch.Tensor:
-    """Raw int32 A = Q_x Q_w^T through the tensor-core GEMM."""
+def convrot_weight_chunks(Q_w: torch.Tensor, kchunk: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Exact-chunk plan of int8 weight codes [N,K]: int32 [ceil(N/128)]."""
+    _need(Q_w, torch.int8, "Q_w")
+    N, K = Q_w.shape
+    if kchunk is None:
+        kchunk = torch.empty(((N + CHUNK_ROWS - 1) // CHUNK_ROWS,), dtype=torch.int32, device=Q_w.device)
+    _check(lib().convrot_weight_chunks(_ptr(Q_w), N, K, _ptr(kchunk), _stream(stream)), "convrot_weight_chunks")
+    return kchunk
+
+
+def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None, kchunk=None) -> torch.Tensor:
+    """Raw int32 A = Q_x Q_w^T through the tensor-core GEMM (optionally with
+    the weight's exact-chunk plan)."""
     _need(Q_x, torch.int8, "Q_x")
     ref = Q_w16 if Q_w16 is not None else Q_w
     M, K = Q_x.shape
@@ -212,23 +225,27 @@ def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None
     if A is None:
         A = torch.empty((M, N), dtype=torch.int32, device=Q_x.device)
     ws = _workspace(int8_linear_workspace_size(M, N, K, Q_w16 is not None), Q_x.device, workspace)
-    _check(lib().int8_gemm_s32(_ptr(Q_x), M, K, _ptr(Q_w), _ptr(Q_w16), N, _ptr(A), _ptr(ws), ws.numel(),
-                               _stream(stream)), "int8_gemm_s32")
+    _check(lib().int8_gemm_s32(_ptr(Q_x), M, K, _ptr(Q_w), _ptr(Q_w16), _ptr(kchunk), N, _ptr(A), _ptr(ws),
+                               ws.numel(), _stream(stream)), "int8_gemm_s32")
     return A
 
 
 def make_weights(q16s: Sequence[torch.Tensor], scales: Sequence[Optional[torch.Tensor]],
-                 biases: Sequence[Optional[torch.Tensor]], Ys: Sequence[torch.Tensor]):
+                 biases: Sequence[Optional[torch.Tensor]], Ys: Sequence[torch.Tensor],
+                 kchunks: Optional[Sequence[Optional[torch.Tensor]]] = None):
+    """The convrot_weight descriptors (kchunks: optional exact-chunk plans)."""
     arr = (convrot_weight * len(q16s))()
-    for j, (q, s, b, y) in enumerate(zip(q16s, scales, biases, Ys)):
-        arr[j] = convrot_weight(_ptr(q), _ptr(s), _ptr(b), q.shape[0], _ptr(y))
+    if kchunks is None:
+        kchunks = [None] * len(q16s)
+    for j, (q, s, b, y, kc) in enumerate(zip(q16s, scales, biases, Ys, kchunks)):
+        arr[j] = convrot_weight(_ptr(q), _ptr(s), _ptr(b), q.shape[0], _ptr(y), _ptr(kc))
     return arr
 
 
 def convrot_linear(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
                    scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
                    Ys: Optional[List[torch.Tensor]] = None, workspace=None, stream=None,
-                   weights=None) -> List[torch.Tensor]:
+                   weights=None, kchunks=None) -> List[torch.Tensor]:
     """Pack X once, then every Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j."""
     xd = _xdtype(X)
     _need(X, X.dtype, "X")
@@ -237,7 +254,7 @@ def convrot_linear(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
         Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
     ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
     if weights is None:
-        weights = make_weights(q16s, scales, biases, Ys)
+        weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear(_ptr(X), xd, M, K, G, weights, len(q16s), _ptr(ws), ws.numel(),
                                 _stream(stream)), "convrot_linear")
     return Ys
@@ -261,7 +278,7 @@ def convrot_pack_activations_f16(X: torch.Tensor, G: int, Q_x16: Optional[torch.
 
 
 def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases,
-                          Ys=None, stream=None, weights=None):
+                          Ys=None, stream=None, weights=None, kchunks=None):
     """Grouped GEMM on an already packed activation (fp16 codes + row scales)."""
     _need(Q_x16, torch.float16, "Q_x16")
     _need(s_x, torch.float32, "s_x")
@@ -269,7 +286,7 @@ def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, 
     if Ys is None:
         Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=Q_x16.device) for q in q16s]
     if weights is None:
-        weights = make_weights(q16s, scales, biases, Ys)
+        weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _stream(stream)),
            "convrot_linear_packed")
     return Ys
@@ -282,8 +299,8 @@ def convrot_linear_host_workspace_size(M: int, K: int, x_dtype: int, n_total: in
 def convrot_linear_host(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
                         scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
                         Ys: Optional[List[torch.Tensor]] = None, chunk_rows: int = 0, workspace=None,
-                        stream=None, copy_in_stream=None, copy_out_stream=None, weights=None
-                        ) -> List[torch.Tensor]:
+                        stream=None, copy_in_stream=None, copy_out_stream=None, weights=None,
+                        kchunks=None) -> List[torch.Tensor]:
     """convrot_linear on host arrays: X [M,K] and the outputs live in (pinned)
     host memory, the weights on the device; transfers of row chunks overlap
     compute on the given copy streams."""
@@ -300,7 +317,7 @@ def convrot_linear_host(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
     n_total = sum(q.shape[0] for q in q16s)
     ws = _workspace(convrot_linear_host_workspace_size(M, K, xd, n_total, chunk_rows), dev, workspace)
     if weights is None:
-        weights = make_weights(q16s, scales, biases, Ys)
+        weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear_host(X.data_ptr(), xd, M, K, G, weights, len(q16s), chunk_rows, _ptr(ws),
                                      ws.numel(), _stream(stream), _stream(copy_in_stream) if copy_in_stream else None,
                                      _stream(copy_out_stream) if copy_out_stream else None),
@@ -312,7 +329,7 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
                            scales: Sequence[Optional[torch.Tensor]],
                            biases: Sequence[Optional[torch.Tensor]],
                            Ys: Optional[List[torch.Tensor]] = None, stream=None,
-                           weights=None) -> List[torch.Tensor]:
+                           weights=None, kchunks=None) -> List[torch.Tensor]:
     """convrot_linear without a workspace, for callers that cannot allocate
     device memory: the packed activation lives in the library's fixed device
     array (NOALLOC_SCRATCH_BYTES per GPU). Pass preallocated Ys to make the
@@ -323,7 +340,7 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
     if Ys is None:
         Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
     if weights is None:
-        weights = make_weights(q16s, scales, biases, Ys)
+        weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear_noalloc(_ptr(X), xd, M, K, G, weights, len(q16s), _stream(stream)),
            "convrot_linear_noalloc")
     return Ys

@@ -474,3 +474,22 @@ def test_oracle_package_exports():
     for name in ("H4", "hadamard_matrix", "rotate", "quantize_rows", "pack",
                  "prepare_weight", "gemm_s32", "reconstruct", "linear", "gelu"):
         assert hasattr(oracle, name)
+
+
+def test_chunk_plan_reference_rule():
+    """The plan reference (tests/chunk_plan_ref.py) on hand-checkable rows:
+    all-127 rows allow 16 K-blocks exactly (16 * 64 * 127 * 127 < 2^24 but
+    17 blocks would not), all-1 rows allow the whole K."""
+    import numpy as np
+    from chunk_plan_ref import plan, plan_is_safe
+    K = 64 * 48
+    full = np.full((128, K), 127, np.int8)
+    assert plan(full).tolist() == [16]
+    assert 127 * 127 * 64 * 16 <= (1 << 24) - 1 < 127 * 127 * 64 * 17
+    ones = np.ones((130, K), np.int8)
+    assert plan(ones).tolist() == [48, 48]
+    mixed = ones.copy()
+    mixed[129] = 127       # the second block holds a dense row
+    p = plan(mixed)
+    assert p.tolist() == [48, 16] and plan_is_safe(mixed, p)
+    assert not plan_is_safe(full, np.array([32], np.int32))
