@@ -51,7 +51,6 @@ __device__ int g_device_error = 0;
 
 namespace {
 
-constexpr int BN = 256;               // activation rows per tile (MMA N)
 constexpr int BK = 64;                // K per pipeline stage: 64 fp16 = 128 B
 constexpr int KB_PER_CHUNK = 16;      // 16 x 64 = 1024 products per exact chunk
 constexpr int UMMA_K = 16;            // K of one kind::f16 MMA
@@ -60,22 +59,23 @@ constexpr int NUM_EPI_WARPS = 8;
 constexpr int PRODUCER_WARP = NUM_EPI_WARPS;
 constexpr int MMA_WARP = NUM_EPI_WARPS + 1;
 constexpr int THREADS = (NUM_EPI_WARPS + 2) * 32;
-constexpr int TMEM_COLS = 2 * BN;     // two fp32 accumulators of BN columns
+constexpr int TMEM_COLS = 512;       // two fp32 accumulators of BN columns each
 constexpr int MAX_LIN = CONVROT_MAX_LINEARS;
-constexpr int COLS_PER_THREAD = BN / 2;   // two epilogue warpgroups split the columns
 constexpr int RASTER_BANDS = 8;       // activation bands per raster group
 
 static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
 
-template <int CG>
+template <int CG, int BN_>
 struct Geom {
+  static constexpr int BN = BN_;                      // activation rows per tile (MMA N)
+  static constexpr int COLS = BN / 2;                 // columns per epilogue thread (two warpgroups)
   static constexpr int TILE_M = CTA_M * CG;           // weight rows per tile (MMA M)
   static constexpr int X_ROWS = BN / CG;              // activation rows each CTA loads
   static constexpr int W_BYTES = CTA_M * BK * 2;
   static constexpr int X_BYTES = X_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = W_BYTES + X_BYTES;
-  static constexpr int STAGES = (CG == 1) ? 4 : 6;
+  static constexpr int STAGES = (196 * 1024) / STAGE_BYTES;  // 4 (CG 1), 6-8 (pairs)
   static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN);
   // shared-memory layout (after aligning the base to 1024 B)
   static constexpr int SMEM_BARS = STAGES * STAGE_BYTES;  // full[S], empty[S], tfull[2], tempty[2], drain
@@ -85,7 +85,10 @@ struct Geom {
   // every operand read of the last stage stays inside the allocation
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024 + (CG == 2 ? X_BYTES : 0);
 };
-static_assert(Geom<1>::SMEM_ALLOC <= 227 * 1024 && Geom<2>::SMEM_ALLOC <= 227 * 1024, "shared memory");
+static_assert(Geom<1, 256>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 256>::SMEM_ALLOC <= 227 * 1024 &&
+                  Geom<2, 192>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 128>::SMEM_ALLOC <= 227 * 1024,
+              "shared memory");
+static_assert(2 * 256 <= TMEM_COLS, "two accumulators fit in TMEM");
 
 struct GemmParams {
   CUtensorMap tmap_x;              // activation codes, fp16 [M, K], box X_ROWS x 64
@@ -100,7 +103,7 @@ struct GemmParams {
   int M;
   int K;
   int num_kb;                      // ceil(K / BK)
-  int n_xtiles;                    // ceil(M / BN)
+  int n_xtiles;                    // ceil(M / BN) activation bands
   int n_wtiles;                    // sum over linears of ceil(N_j / TILE_M)
   int total_tiles;
   int n_lin;
@@ -148,10 +151,12 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
   return max(1, min(L, p.num_kb));
 }
 
-template <int CG>
+template <int CG, int BN_>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Gm = Geom<CG>;
+  using Gm = Geom<CG, BN_>;
+  constexpr int BN = Gm::BN;
+  constexpr int COLS_PER_THREAD = Gm::COLS;
   constexpr int STAGES = Gm::STAGES;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -400,10 +405,10 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
   return CONVROT_OK;
 }
 
-template <int CG>
+template <int CG, int BN>
 int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32) {
-  using Gm = Geom<CG>;
+  using Gm = Geom<CG, BN>;
   memset(&p, 0, sizeof(p));
   int st = make_tmap(&p.tmap_x, x16, M, K, Gm::X_ROWS);
   if (st) return st;
@@ -435,7 +440,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
 }
 
 // Raise the kernel's shared-memory limit once per device.
-template <int CG>
+template <int CG, int BN>
 int configure_kernel() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -444,15 +449,32 @@ int configure_kernel() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Geom<CG>::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Geom<CG, BN>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
   }
   return CONVROT_OK;
 }
 
-// Co-resident CTA pairs on the current device (0 if pairs cannot launch), cached per device.
+cudaLaunchConfig_t pair_config(int n_pairs, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * n_pairs, 1, 1);
+  cfg.blockDim = dim3(THREADS, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+// Co-resident CTA pairs of the BN variant on the current device (0 if pairs
+// cannot launch), cached per device. The kernel must be configured first.
+template <int BN>
 int max_pairs() {
   static std::mutex mu;
   static int cached[64];
@@ -461,19 +483,10 @@ int max_pairs() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!known[dev]) {
-    cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * device_sm_count(), 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Geom<2>::SMEM_ALLOC;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cudaLaunchConfig_t cfg = pair_config(device_sm_count(), Geom<2, BN>::SMEM_ALLOC, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the sticky launch-query error
       n = 0;
     }
@@ -481,6 +494,20 @@ int max_pairs() {
     known[dev] = true;
   }
   return cached[dev];
+}
+
+template <int BN>
+int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
+                 bool raw_s32, int pairs, cudaStream_t stream) {
+  GemmParams p;
+  if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
+  if (p.total_tiles == 0) return CONVROT_OK;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg =
+      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN>::SMEM_ALLOC, stream, attr);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN>, p);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return check_launch();
 }
 
 // ---------------------------------------------------------------------------
@@ -560,37 +587,43 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+// Activation rows per tile: the tile height among 256, 192 and 128 whose
+// last wave of pair tiles is least empty. Modelled time: waves x (BN + 32),
+// the 32 standing for the fixed cost of a tile; ties go to the taller tile.
+int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs) {
+  int64_t wtiles = 0;
+  for (int j = 0; j < n_lin; ++j) wtiles += (lins[j].N + 2 * CTA_M - 1) / (2 * CTA_M);
+  int best = 256;
+  int64_t best_cost = -1;
+  for (int bn : {256, 192, 128}) {
+    const int64_t tiles = ((M + bn - 1) / bn) * wtiles;
+    const int64_t waves = (tiles + pairs - 1) / pairs;
+    const int64_t cost = waves * (bn + 32);
+    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+  }
+  return best;
+}
+
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream) {
   if (M == 0) return CONVROT_OK;
-  GemmParams p;
-  if (int st = configure_kernel<2>()) return st;
-  const int pairs = max_pairs();
+  if (int st = configure_kernel<2, 256>()) return st;
+  if (int st = configure_kernel<2, 192>()) return st;
+  if (int st = configure_kernel<2, 128>()) return st;
+  const int pairs = std::min(max_pairs<256>(), std::min(max_pairs<192>(), max_pairs<128>()));
   if (pairs > 0) {
-    if (int st = fill_params<2>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
-    if (p.total_tiles == 0) return CONVROT_OK;
-    const int n = std::min(p.total_tiles, pairs);
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(2 * n, 1, 1);
-    cfg.blockDim = dim3(THREADS, 1, 1);
-    cfg.dynamicSmemBytes = Geom<2>::SMEM_ALLOC;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2>, p);
-    if (e != cudaSuccess) return set_cuda_error(e);
-    return check_launch();
+    switch (pick_tile_rows(M, lins, n_lin, pairs)) {
+      case 128: return launch_pairs<128>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      case 192: return launch_pairs<192>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      default: return launch_pairs<256>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    }
   }
-  if (int st = configure_kernel<1>()) return st;
-  if (int st = fill_params<1>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
+  GemmParams p;
+  if (int st = configure_kernel<1, 256>()) return st;
+  if (int st = fill_params<1, 256>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
   const int grid = std::min(p.total_tiles, device_sm_count());
-  convrot_gemm_kernel<1><<<grid, THREADS, Geom<1>::SMEM_ALLOC, stream>>>(p);
+  convrot_gemm_kernel<1, 256><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
   return check_launch();
 }
 
