@@ -82,6 +82,12 @@ typedef enum convrot_dtype {
   CONVROT_F16 = 1  /* IEEE binary16 (converted exactly to fp32 on load) */
 } convrot_dtype;
 
+/* Activation applied to a linear's output (convrot_mlp). */
+typedef enum convrot_activation {
+  CONVROT_ACT_NONE = 0,
+  CONVROT_ACT_GELU = 1 /* 0.5 y (1 + erf(y / sqrt 2)), fp32, after the bias */
+} convrot_activation;
+
 /* Longest activation row (K) the pack kernel holds on chip. */
 #define CONVROT_PACK_MAX_K 32768
 /* Largest K whose worst-case int32 accumulation fits: 133144 * 127^2 < 2^31. */
@@ -262,6 +268,31 @@ int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, i
                         const convrot_weight* weights, int n_weights, int64_t chunk_rows,
                         void* workspace, size_t workspace_bytes, void* stream,
                         void* copy_in_stream, void* copy_out_stream);
+
+/* Device bytes convrot_mlp needs: both packed activations and H. */
+size_t convrot_mlp_workspace_size(int64_t M, int64_t K, int64_t N_up);
+
+/*
+ * convrot_mlp -- an up linear, an activation and a down linear on the device
+ * (the transformer MLP built from two convrot linears):
+ *   H = act(float(Q_x Q_up^T) * s_x * s_up + b_up)   (activation in the up
+ *       GEMM's epilogue, after the bias; H fp32 [M, N_up]),
+ *   Y = float(Q_h Q_down^T) * s_h * s_down + b_down  (H packed with G_down).
+ *   X        [M,K] fp32/fp16 activations.
+ *   up       weight of the up linear: q16 [N_up,K], scale, bias, kchunk as in
+ *            convrot_linear; Y = NULL (H stays in the workspace) or an fp32
+ *            [M,N_up] device array that receives H.
+ *   activation  CONVROT_ACT_NONE or CONVROT_ACT_GELU.
+ *   down     weight of the down linear: q16 [N_down,N_up], ...; Y [M,N_down].
+ *   G_up / G_down  group sizes (4^n) dividing K / N_up.
+ *   workspace  >= convrot_mlp_workspace_size(M, K, N_up) bytes.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_WORKSPACE,
+ *         ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int G_up,
+                const convrot_weight* up, int activation, int G_down,
+                const convrot_weight* down, void* workspace, size_t workspace_bytes,
+                void* stream);
 
 /* Size of the fixed device array that convrot_linear_noalloc uses (32 MiB). */
 #define CONVROT_NOALLOC_SCRATCH_BYTES (32u << 20)

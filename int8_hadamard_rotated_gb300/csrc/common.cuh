@@ -373,6 +373,7 @@ struct GemmLinear {
   void* out;           // [M,N] fp32 Y or int32 A
   int64_t N;
   const int32_t* kchunk;  // [ceil(N/128)] exact-chunk plan (64-wide K blocks per chunk) or null
+  int act = CONVROT_ACT_NONE;  // activation applied to Y after the bias
 };
 
 // Exact-chunk plan of int8 weight codes (see convrot_weight_chunks).

@@ -96,6 +96,7 @@ struct GemmParams {
   const float* s_w[MAX_LIN];
   const float* bias[MAX_LIN];
   const int32_t* kchunk[MAX_LIN];  // exact-chunk plan per 128 weight rows, or null
+  int act[MAX_LIN];                // CONVROT_ACT_* applied after the bias
   void* out[MAX_LIN];              // fp32 Y_j or int32 A_j, [M, N_j]
   int N[MAX_LIN];
   int wtile_start[MAX_LIN + 1];    // prefix sums of weight tiles (TILE_M rows) per linear
@@ -133,6 +134,12 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   c.lin = j;
   c.wt = w - p.wtile_start[j];
   return c;
+}
+
+// GELU with the error function, 0.5 y (1 + erf(y / sqrt 2)), in fp32 with
+// CUDA's erff (the MLP activation between an up and a down linear).
+__device__ __forceinline__ float gelu_erf(float y) {
+  return __fmul_rn(__fmul_rn(0.5f, y), __fadd_rn(1.0f, erff(__fmul_rn(y, 0.70710678118654752f))));
 }
 
 // K blocks (of BK) per exact fp32 chunk for a tile: the weight's plan for the
@@ -361,6 +368,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const float* b_ptr = p.bias[c.lin];
         const float sw = (o_ok && sw_ptr) ? __ldg(sw_ptr + o) : 1.0f;
         const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
+        const int act = p.act[c.lin];
 #pragma unroll
         for (int i = 0; i < COLS_PER_THREAD; ++i) {
           const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
@@ -370,6 +378,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             float y = __fmul_rn(__int2float_rn(acc[i]), sx);
             if (sw_ptr) y = __fmul_rn(y, sw);
             if (b_ptr) y = __fadd_rn(y, bb);
+            if (act == CONVROT_ACT_GELU) y = gelu_erf(y);
             st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
           }
         }
@@ -419,6 +428,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
     p.s_w[j] = lins[j].s_w;
     p.bias[j] = lins[j].bias;
     p.kchunk[j] = lins[j].kchunk;
+    p.act[j] = lins[j].act;
     p.out[j] = lins[j].out;
     p.N[j] = static_cast<int>(lins[j].N);
     p.wtile_start[j] = wt;

@@ -32,6 +32,9 @@ ERR_CUDA = 9
 ERR_DEVICE = 10
 ERR_SCRATCH = 11
 
+ACT_NONE = 0
+ACT_GELU = 1
+
 F32 = 0
 F16 = 1
 MAX_LINEARS = 8
@@ -77,6 +80,9 @@ SIGNATURES = {
     "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
     "convrot_linear_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I64, _VP, _SZ,
                                  _VP, _VP, _VP]),
+    "convrot_mlp_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "convrot_mlp": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I,
+                         ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_device_status": (_I, [_VP]),
 }
@@ -323,6 +329,34 @@ def convrot_linear_host(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
                                      _stream(copy_out_stream) if copy_out_stream else None),
            "convrot_linear_host")
     return Ys
+
+
+def convrot_mlp_workspace_size(M: int, K: int, N_up: int) -> int:
+    return int(lib().convrot_mlp_workspace_size(M, K, N_up))
+
+
+def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: int, down: Tuple,
+                Y: Optional[torch.Tensor] = None, H: Optional[torch.Tensor] = None, workspace=None,
+                stream=None) -> torch.Tensor:
+    """Up linear, activation, down linear on the device. `up` and `down` are
+    (q16, scale, bias, kchunk) tuples; H (optional, fp32 [M, N_up]) receives
+    the activated up output."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    uq, us, ub, uk = up
+    dq, ds, db, dk = down
+    N_up, N_down = uq.shape[0], dq.shape[0]
+    if Y is None:
+        Y = torch.empty((M, N_down), dtype=torch.float32, device=X.device)
+    if H is not None:
+        _need(H, torch.float32, "H")
+    wu = (convrot_weight * 1)(convrot_weight(_ptr(uq), _ptr(us), _ptr(ub), N_up, _ptr(H), _ptr(uk)))
+    wd = (convrot_weight * 1)(convrot_weight(_ptr(dq), _ptr(ds), _ptr(db), N_down, _ptr(Y), _ptr(dk)))
+    ws = _workspace(convrot_mlp_workspace_size(M, K, N_up), X.device, workspace)
+    _check(lib().convrot_mlp(_ptr(X), xd, M, K, G_up, wu, activation, G_down, wd, _ptr(ws), ws.numel(),
+                             _stream(stream)), "convrot_mlp")
+    return Y
 
 
 def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
