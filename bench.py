@@ -375,6 +375,35 @@ def run_gpu(args, rank, world, local_rank):
              "bytes": large_bytes, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
     del Xl, Ql, sl
 
+    # ---- the DiT MLP pair on the device (convrot_mlp) ---------------------
+    mw = workloads.get("dit_mlp")
+    mcase = workloads.make_case(mw)
+    Xm = torch.from_numpy(mcase.X).to(dev)
+    mlp_w = []
+    for W, b in zip(mcase.Ws, mcase.bs):
+        q8, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), mw.G)
+        mlp_w.append((q16, s_w, torch.from_numpy(b).to(dev), ops.convrot_weight_chunks(q8)))
+        del q8
+    Ym = torch.empty((mw.M, mw.Ns[1]), dtype=torch.float32, device=dev)
+    wsm = torch.empty((ops.convrot_mlp_workspace_size(mw.M, mw.K, mw.Ns[0]),), dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        ops.convrot_mlp(Xm, mw.G, mlp_w[0], ops.ACT_GELU, mw.G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
+    mt = []
+    for _ in range(10):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        ops.convrot_mlp(Xm, mw.G, mlp_w[0], ops.ACT_GELU, mw.G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
+        b.record(stream)
+        mt.append((a, b))
+    torch.cuda.synchronize()
+    mms = float(np.mean([a.elapsed_time(b) for a, b in mt]))
+    mlp = {"workload": f"dit_mlp: X fp32 [{mw.M},{mw.K}] -> up [{mw.Ns[0]},{mw.K}] + GELU -> repack -> "
+                       f"down [{mw.Ns[1]},{mw.Ns[0]}], G={mw.G}, one convrot_mlp call",
+           "ms": round(mms, 4), "TOPS": round(mw.gemm_ops / (mms * 1e-3) / 1e12, 2),
+           "ops_per_call": int(mw.gemm_ops)}
+    del Xm, mlp_w, Ym, wsm
+
     pack = {
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
         "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
@@ -391,7 +420,7 @@ def run_gpu(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": data_desc(w), "config": config_dict(w, world),
-        "roofline": roofline, "pack": pack, "e2e": e2e,
+        "roofline": roofline, "pack": pack, "mlp_chain": mlp, "e2e": e2e,
         "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "timing": {"step_ms_median": float(np.median(step_ms)), "pack_us_mean": float(pack_ms.mean() * 1e3),

@@ -85,7 +85,7 @@ typedef enum convrot_dtype {
 /* Activation applied to a linear's output (convrot_mlp). */
 typedef enum convrot_activation {
   CONVROT_ACT_NONE = 0,
-  CONVROT_ACT_GELU = 1 /* 0.5 y (1 + erf(y / sqrt 2)), fp32, after the bias */
+  CONVROT_ACT_GELU = 1 /* 0.5 y (1 + erf(y / sqrt 2)), fp32 with erff */
 } convrot_activation;
 
 /* Longest activation row (K) the pack kernel holds on chip. */
@@ -204,6 +204,22 @@ int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                    void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * convrot_linear_scaled -- convrot_linear for linears with an input scale
+ * ("Runtime activation quantization": for input scales other than 1 the
+ * activations are scaled before the convrot quantization and the output is
+ * unscaled before the bias is added):
+ *   X' = fp32(input_scale * X),  packed with G,
+ *   Y_j = (((float(Q_x' Q_wj^T) * s_x') * s_wj) / input_scale) + b_j,
+ * each operation one fp32 rounding. Linears sharing X, G and the input scale
+ * share the packed activation. input_scale = 1 is exactly convrot_linear.
+ *   input_scale  finite and > 0 (else ERR_ARG); other arguments as convrot_linear.
+ * Errors: as convrot_linear.
+ */
+int convrot_linear_scaled(const void* X, int x_dtype, int64_t M, int64_t K, int G,
+                          float input_scale, const convrot_weight* weights, int n_weights,
+                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * int8_gemm_s32 -- the raw int32 product A = Q_x Q_w^T (no scales), through
  * the same tensor-core GEMM as int8_linear. For exactness checks.
  *   Arguments as int8_linear; kchunk: the weight's exact-chunk plan
@@ -275,13 +291,13 @@ size_t convrot_mlp_workspace_size(int64_t M, int64_t K, int64_t N_up);
 /*
  * convrot_mlp -- an up linear, an activation and a down linear on the device
  * (the transformer MLP built from two convrot linears):
- *   H = act(float(Q_x Q_up^T) * s_x * s_up + b_up)   (activation in the up
- *       GEMM's epilogue, after the bias; H fp32 [M, N_up]),
+ *   Y_up = float(Q_x Q_up^T) * s_x * s_up + b_up       (fp32 [M, N_up]),
+ *   H = act(Y_up), applied elementwise as Y_up is loaded for the pack,
  *   Y = float(Q_h Q_down^T) * s_h * s_down + b_down  (H packed with G_down).
  *   X        [M,K] fp32/fp16 activations.
  *   up       weight of the up linear: q16 [N_up,K], scale, bias, kchunk as in
- *            convrot_linear; Y = NULL (H stays in the workspace) or an fp32
- *            [M,N_up] device array that receives H.
+ *            convrot_linear; Y = NULL (Y_up stays in the workspace) or an fp32
+ *            [M,N_up] device array that receives Y_up (before the activation).
  *   activation  CONVROT_ACT_NONE or CONVROT_ACT_GELU.
  *   down     weight of the down linear: q16 [N_down,N_up], ...; Y [M,N_down].
  *   G_up / G_down  group sizes (4^n) dividing K / N_up.

@@ -259,13 +259,13 @@ int check_weight_list(const convrot_weight* weights, int n_weights) {
 }
 
 int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                   const convrot_weight* weights, int n_weights, cudaStream_t s) {
+                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale) {
   GemmLinear lins[CONVROT_MAX_LINEARS];
   int n = 0;
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N, w.kchunk};
+    lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N, w.kchunk, in_scale};
   }
   if (n == 0) return CONVROT_OK;
   return launch_gemm(x16, s_x, M, K, lins, n, false, s);
@@ -323,7 +323,15 @@ int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, in
 int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                    const convrot_weight* weights, int n_weights,
                    void* workspace, size_t workspace_bytes, void* stream) {
+  return convrot_linear_scaled(X, x_dtype, M, K, G, 1.0f, weights, n_weights, workspace, workspace_bytes,
+                               stream);
+}
+
+int convrot_linear_scaled(const void* X, int x_dtype, int64_t M, int64_t K, int G, float input_scale,
+                          const convrot_weight* weights, int n_weights,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   if (M < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (!(input_scale > 0.0f) || !(input_scale <= 3.402823466e38f)) return CONVROT_ERR_ARG;  // finite, > 0
   if (x_dtype != CONVROT_F32 && x_dtype != CONVROT_F16) return CONVROT_ERR_ARG;
   if (int st = check_weight_list(weights, n_weights)) return st;
   if (M == 0) return CONVROT_OK;
@@ -349,9 +357,9 @@ int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   __half* x16 = reinterpret_cast<__half*>(ws);
   float* s_x = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(M) * K * 2));
-  int st = launch_pack(X, x_dtype, M, K, G, x16, kPackF16, s_x, s);
+  int st = launch_pack(X, x_dtype, M, K, G, x16, kPackF16, s_x, s, input_scale);
   if (st) return st;
-  return launch_grouped(x16, s_x, M, K, weights, n_weights, s);
+  return launch_grouped(x16, s_x, M, K, weights, n_weights, s, input_scale);
 }
 
 int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, void* stream) {

@@ -360,8 +360,14 @@ bool device_is_sm103();
 enum PackOut { kPackI8 = 0, kPackF16 = 1 };
 
 // Rotate + quantize rows of X. out_codes is int8 (kPackI8) or fp16 (kPackF16).
+// in_scale multiplies every element before the rotation (1 = the plain pack).
 int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
-                void* out_codes, int out_kind, float* scales, cudaStream_t stream);
+                void* out_codes, int out_kind, float* scales, cudaStream_t stream, float in_scale = 1.0f);
+
+// The same pack of fp32 rows into binary16 codes with GELU applied to every
+// element as it is loaded (the MLP's activation, fused into its repack).
+int launch_pack_gelu(const float* X, int64_t M, int64_t K, int G, __half* out_codes, float* scales,
+                     cudaStream_t stream);
 
 // int8 codes -> fp16 codes (exact), n elements, n % 16 == 0.
 int launch_widen(const int8_t* src, __half* dst, int64_t n, cudaStream_t stream);
@@ -373,7 +379,7 @@ struct GemmLinear {
   void* out;           // [M,N] fp32 Y or int32 A
   int64_t N;
   const int32_t* kchunk;  // [ceil(N/128)] exact-chunk plan (64-wide K blocks per chunk) or null
-  int act = CONVROT_ACT_NONE;  // activation applied to Y after the bias
+  float in_scale = 1.0f;       // the activations were packed times this; Y is divided by it before the bias
 };
 
 // Exact-chunk plan of int8 weight codes (see convrot_weight_chunks).
@@ -395,6 +401,6 @@ int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64
                   const void* in0, size_t n0, const void* in1, size_t n1);
 // One grouped GEMM over the non-empty linears, on packed fp16 codes + s_x.
 int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                   const convrot_weight* weights, int n_weights, cudaStream_t s);
+                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale = 1.0f);
 
 }  // namespace convrot

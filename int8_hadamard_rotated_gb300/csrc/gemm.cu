@@ -96,7 +96,7 @@ struct GemmParams {
   const float* s_w[MAX_LIN];
   const float* bias[MAX_LIN];
   const int32_t* kchunk[MAX_LIN];  // exact-chunk plan per 128 weight rows, or null
-  int act[MAX_LIN];                // CONVROT_ACT_* applied after the bias
+  float in_scale[MAX_LIN];         // input scale to divide out before the bias (1 = none)
   void* out[MAX_LIN];              // fp32 Y_j or int32 A_j, [M, N_j]
   int N[MAX_LIN];
   int wtile_start[MAX_LIN + 1];    // prefix sums of weight tiles (TILE_M rows) per linear
@@ -136,12 +136,6 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   return c;
 }
 
-// GELU with the error function, 0.5 y (1 + erf(y / sqrt 2)), in fp32 with
-// CUDA's erff (the MLP activation between an up and a down linear).
-__device__ __forceinline__ float gelu_erf(float y) {
-  return __fmul_rn(__fmul_rn(0.5f, y), __fadd_rn(1.0f, erff(__fmul_rn(y, 0.70710678118654752f))));
-}
-
 // K blocks (of BK) per exact fp32 chunk for a tile: the weight's plan for the
 // tile's 128-row blocks (their minimum), or KB_PER_CHUNK (1024 products,
 // always exact) without a plan.
@@ -158,7 +152,9 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
   return max(1, min(L, p.num_kb));
 }
 
-template <int CG, int BN_>
+// UNSCALE: the variant for linears with an input scale other than 1 (the IEEE
+// division stays out of the common kernel's unrolled epilogue).
+template <int CG, int BN_, bool UNSCALE>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   using Gm = Geom<CG, BN_>;
@@ -368,7 +364,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const float* b_ptr = p.bias[c.lin];
         const float sw = (o_ok && sw_ptr) ? __ldg(sw_ptr + o) : 1.0f;
         const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
-        const int act = p.act[c.lin];
+        const float in_scale = UNSCALE ? p.in_scale[c.lin] : 1.0f;
 #pragma unroll
         for (int i = 0; i < COLS_PER_THREAD; ++i) {
           const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
@@ -377,8 +373,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             // float(A) * s_x * s_w + b, one rounding per operation, in that order
             float y = __fmul_rn(__int2float_rn(acc[i]), sx);
             if (sw_ptr) y = __fmul_rn(y, sw);
+            if (UNSCALE) y = __fdiv_rn(y, in_scale);  // unscale before the bias
             if (b_ptr) y = __fadd_rn(y, bb);
-            if (act == CONVROT_ACT_GELU) y = gelu_erf(y);
             st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
           }
         }
@@ -428,7 +424,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
     p.s_w[j] = lins[j].s_w;
     p.bias[j] = lins[j].bias;
     p.kchunk[j] = lins[j].kchunk;
-    p.act[j] = lins[j].act;
+    p.in_scale[j] = lins[j].in_scale;
     p.out[j] = lins[j].out;
     p.N[j] = static_cast<int>(lins[j].N);
     p.wtile_start[j] = wt;
@@ -450,7 +446,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
 }
 
 // Raise the kernel's shared-memory limit once per device.
-template <int CG, int BN>
+template <int CG, int BN, bool UNSCALE>
 int configure_kernel() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -459,7 +455,7 @@ int configure_kernel() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Geom<CG, BN>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
@@ -496,7 +492,7 @@ int max_pairs() {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = pair_config(device_sm_count(), Geom<2, BN>::SMEM_ALLOC, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the sticky launch-query error
       n = 0;
     }
@@ -506,7 +502,7 @@ int max_pairs() {
   return cached[dev];
 }
 
-template <int BN>
+template <int BN, bool UNSCALE>
 int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
                  bool raw_s32, int pairs, cudaStream_t stream) {
   GemmParams p;
@@ -515,7 +511,8 @@ int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, cons
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
       pair_config(std::min(p.total_tiles, pairs), Geom<2, BN>::SMEM_ALLOC, stream, attr);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN>, p);
+  if (int st = configure_kernel<2, BN, UNSCALE>()) return st;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
   return check_launch();
 }
@@ -617,23 +614,34 @@ int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs) {
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream) {
   if (M == 0) return CONVROT_OK;
-  if (int st = configure_kernel<2, 256>()) return st;
-  if (int st = configure_kernel<2, 192>()) return st;
-  if (int st = configure_kernel<2, 128>()) return st;
+  bool unscale = false;
+  for (int j = 0; j < n_lin; ++j) unscale |= (lins[j].in_scale != 1.0f);
+  if (int st = configure_kernel<2, 256, false>()) return st;
+  if (int st = configure_kernel<2, 192, false>()) return st;
+  if (int st = configure_kernel<2, 128, false>()) return st;
   const int pairs = std::min(max_pairs<256>(), std::min(max_pairs<192>(), max_pairs<128>()));
   if (pairs > 0) {
-    switch (pick_tile_rows(M, lins, n_lin, pairs)) {
-      case 128: return launch_pairs<128>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      case 192: return launch_pairs<192>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      default: return launch_pairs<256>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    const int bn = pick_tile_rows(M, lins, n_lin, pairs);
+    if (unscale) {
+      if (bn == 128) return launch_pairs<128, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      if (bn == 192) return launch_pairs<192, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      return launch_pairs<256, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
     }
+    if (bn == 128) return launch_pairs<128, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    if (bn == 192) return launch_pairs<192, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    return launch_pairs<256, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
   }
   GemmParams p;
-  if (int st = configure_kernel<1, 256>()) return st;
   if (int st = fill_params<1, 256>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
   const int grid = std::min(p.total_tiles, device_sm_count());
-  convrot_gemm_kernel<1, 256><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
+  if (unscale) {
+    if (int st = configure_kernel<1, 256, true>()) return st;
+    convrot_gemm_kernel<1, 256, true><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
+  } else {
+    if (int st = configure_kernel<1, 256, false>()) return st;
+    convrot_gemm_kernel<1, 256, false><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
+  }
   return check_launch();
 }
 

@@ -1,11 +1,12 @@
 // mlp.cu -- convrot_mlp: an up linear, its activation, and a down linear,
 // entirely on the device.
 //
-// X is packed once for the up linear; the up GEMM applies the activation in
-// its epilogue (after the bias) and writes H = act(Y_up) in fp32; H is packed
-// with the down linear's group size and the down GEMM writes Y. H and both
-// packed activations live in the caller's workspace (or H in the caller's
-// array), so nothing goes through the host between the two linears.
+// X is packed once for the up linear and the up GEMM writes Y_up in fp32; the
+// activation is applied as Y_up is loaded by the pack for the down linear (the
+// pack's prologue), so H = act(Y_up) is never stored, and the down GEMM writes
+// Y. Y_up and both packed activations live in the caller's workspace (or Y_up
+// in the caller's array), so nothing goes through the host between the two
+// linears.
 #include "common.cuh"
 
 namespace convrot {
@@ -75,10 +76,12 @@ extern "C" int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int
   __half* h16 = reinterpret_cast<__half*>(ws + l.h16);
   float* s_h = reinterpret_cast<float*>(ws + l.s_h);
   if (int st = launch_pack(X, x_dtype, M, K, G_up, x16, kPackF16, s_x, s)) return st;
-  GemmLinear lu{reinterpret_cast<const __half*>(up->q16), up->scale, up->bias, H, N_up, up->kchunk, activation};
+  GemmLinear lu{reinterpret_cast<const __half*>(up->q16), up->scale, up->bias, H, N_up, up->kchunk};
   if (int st = launch_gemm(x16, s_x, M, K, &lu, 1, false, s)) return st;
-  if (int st = launch_pack(H, CONVROT_F32, M, N_up, G_down, h16, kPackF16, s_h, s)) return st;
+  int st = (activation == CONVROT_ACT_GELU) ? launch_pack_gelu(H, M, N_up, G_down, h16, s_h, s)
+                                             : launch_pack(H, CONVROT_F32, M, N_up, G_down, h16, kPackF16, s_h, s);
+  if (st) return st;
   GemmLinear ld{reinterpret_cast<const __half*>(down->q16), down->scale, down->bias, down->Y, down->N,
-                down->kchunk, CONVROT_ACT_NONE};
+                down->kchunk};
   return launch_gemm(h16, s_h, M, N_up, &ld, 1, false, s);
 }

@@ -391,13 +391,35 @@ __device__ __forceinline__ int out_unit(int u, int gi, int li, int j) {
   return gi * 64 + swap2(j) * 16 + swap_digit_bits4(li);
 }
 
+// An input scale other than 1: every element is multiplied by it (one fp32
+// rounding) before the rotation.
+__device__ __forceinline__ void scale_unit(float (&v)[16], float a) {
+#pragma unroll
+  for (int p = 0; p < 16; ++p) v[p] = __fmul_rn(v[p], a);
+}
+
+// Elementwise prologue applied to the loaded row before everything else:
+// none, or GELU 0.5 x (1 + erf(x / sqrt 2)) in fp32 with CUDA's erff (the MLP
+// activation, applied where its output is quantized for the down linear).
+constexpr int kProNone = 0;
+constexpr int kProGelu = 1;
+
+template <int PRO>
+__device__ __forceinline__ void prologue_unit(float (&v)[16]) {
+  if (PRO == kProGelu) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p)
+      v[p] = __fmul_rn(__fmul_rn(0.5f, v[p]), __fadd_rn(1.0f, erff(__fmul_rn(v[p], 0.70710678118654752f))));
+  }
+}
+
 // ---- pack_kernel: the general path (per-thread cp.async) ---------------------
 
 // One CTA handles `rpc` rows with `tpr` threads each per block, persistently.
-template <int G, typename TIn, int OUT>
+template <int G, typename TIn, int OUT, int PRO>
 __global__ void __launch_bounds__(kMaxThreads)
 pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64_t nblocks,
-            int two_stage, void* __restrict__ out_codes, float* __restrict__ scales) {
+            int two_stage, float in_scale, void* __restrict__ out_codes, float* __restrict__ scales) {
   using C = Geo<G>;
   constexpr int CPU = InTraits<TIn>::kChunksPerUnit;
   constexpr int CH = 4 * CPU;  // 16-byte chunks per thread per stage
@@ -469,6 +491,8 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
 #pragma unroll
       for (int k = 0; k < CPU; ++k) c[k] = stage_buf[(stage * CH + j * CPU + k) * nth + tid];
       unit_to_f32<TIn>(c, v[j]);
+      prologue_unit<PRO>(v[j]);
+      if (in_scale != 1.0f) scale_unit(v[j], in_scale);
     }
     rotate64<G>(v, ls);
 
@@ -519,6 +543,7 @@ struct PackTmaParams {
   CUtensorMap tmap;     // X as [M][L][E] elements (E per 128-B line), box {E, Lb, rbox}, 128-B swizzle
   void* out;            // codes [M, K], int8 or binary16
   float* scales;        // [M]
+  float in_scale;       // input scale applied before the rotation (1 = none)
   int64_t M;
   int64_t nblocks;      // ceil(M / R)
   int K;
@@ -538,7 +563,7 @@ struct PackTmaParams {
 //   [kTmaMaxStages] u64     "stage full" barriers
 //   [2][R] u64              tagged row absmax
 //   int                     abort flag
-template <int G, typename TIn, int OUT>
+template <int G, typename TIn, int OUT, int PRO>
 __global__ void __launch_bounds__(kMaxThreads)
 pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   using C = Geo<G>;
@@ -578,6 +603,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   __syncthreads();
 
   const uint64_t pol_in = l2_policy_evict_first();
+  const float in_scale = p.in_scale;
   const uint32_t block_bytes = static_cast<uint32_t>(R) * static_cast<uint32_t>(p.L) * 128u;
   // Thread 0 only: load block `blk` into stage `stage`.
   auto issue = [&](int64_t blk, int stage) {
@@ -642,6 +668,8 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
         for (int k = 0; k < CPU; ++k) c[k] = make_uint4(0u, 0u, 0u, 0u);
       }
       unit_to_f32<TIn>(c, v[j]);
+      prologue_unit<PRO>(v[j]);
+      if (in_scale != 1.0f) scale_unit(v[j], in_scale);
     }
     rotate64<G>(v, ls);
 
@@ -734,8 +762,9 @@ int ensure_smem(Kern kern, size_t smem, size_t (&configured)[64]) {
   return CONVROT_OK;
 }
 
-template <int G, typename TIn, int OUT>
-int launch_pack_cpasync(const void* X, int64_t M, int K, void* out, float* scales, cudaStream_t stream) {
+template <int G, typename TIn, int OUT, int PRO>
+int launch_pack_cpasync(const void* X, int64_t M, int K, float in_scale, void* out, float* scales,
+                        cudaStream_t stream) {
   const int tpr = (K + 63) / 64;
   int rpc = 32 / gcd_int(tpr, 32);
   int threads = tpr * rpc;
@@ -751,7 +780,7 @@ int launch_pack_cpasync(const void* X, int64_t M, int K, void* out, float* scale
   constexpr size_t kSmemLimit = 200 * 1024;  // leaves room for the static shared memory
   const int two_stage = (static_cast<size_t>(2) * CH * threads * 16 <= kSmemLimit) ? 1 : 0;
   const size_t smem = static_cast<size_t>(two_stage ? 2 : 1) * CH * threads * 16;
-  auto kern = pack_kernel<G, TIn, OUT>;
+  auto kern = pack_kernel<G, TIn, OUT, PRO>;
   static size_t configured[64] = {};
   if (int st = ensure_smem(kern, smem, configured)) return st;
   int per_sm = 0;
@@ -761,7 +790,7 @@ int launch_pack_cpasync(const void* X, int64_t M, int K, void* out, float* scale
   const int64_t nblocks = (M + rpc - 1) / rpc;
   const int64_t grid = std::min<int64_t>(nblocks, static_cast<int64_t>(per_sm) * device_sm_count());
   kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(
-      static_cast<const TIn*>(X), M, K, tpr, rpc, nblocks, two_stage, out, scales);
+      static_cast<const TIn*>(X), M, K, tpr, rpc, nblocks, two_stage, in_scale, out, scales);
   return check_launch();
 }
 
@@ -813,14 +842,15 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
   return true;
 }
 
-template <int G, typename TIn, int OUT>
-int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cudaStream_t stream) {
+template <int G, typename TIn, int OUT, int PRO>
+int launch_pack_t(const void* X, int64_t M, int K, float in_scale, void* out, float* scales,
+                  cudaStream_t stream) {
   PackTmaParams p;
   memset(&p, 0, sizeof(p));
   int threads = 0;
   size_t smem = 0;
   if (!plan_tma<TIn, OUT>(K, p, threads, smem))
-    return launch_pack_cpasync<G, TIn, OUT>(X, M, K, out, scales, stream);
+    return launch_pack_cpasync<G, TIn, OUT, PRO>(X, M, K, in_scale, out, scales, stream);
 
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return set_cuda_error(cudaErrorNotSupported);
@@ -839,10 +869,11 @@ int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cud
   if (r != CUDA_SUCCESS) return set_cuda_error(cudaErrorInvalidValue);
   p.out = out;
   p.scales = scales;
+  p.in_scale = in_scale;
   p.M = M;
   p.nblocks = (M + p.R - 1) / p.R;
 
-  auto kern = pack_tma_kernel<G, TIn, OUT>;
+  auto kern = pack_tma_kernel<G, TIn, OUT, PRO>;
   static size_t configured[64] = {};
   if (int st = ensure_smem(kern, smem, configured)) return st;
   int per_sm = 0;
@@ -854,15 +885,15 @@ int launch_pack_t(const void* X, int64_t M, int K, void* out, float* scales, cud
   return check_launch();
 }
 
-template <typename TIn, int OUT>
-int dispatch_group(const void* X, int64_t M, int K, int G, void* out, float* scales, cudaStream_t s) {
+template <typename TIn, int OUT, int PRO = kProNone>
+int dispatch_group(const void* X, int64_t M, int K, int G, float a, void* out, float* scales, cudaStream_t s) {
   switch (G) {
-    case 1: return launch_pack_t<1, TIn, OUT>(X, M, K, out, scales, s);
-    case 4: return launch_pack_t<4, TIn, OUT>(X, M, K, out, scales, s);
-    case 16: return launch_pack_t<16, TIn, OUT>(X, M, K, out, scales, s);
-    case 64: return launch_pack_t<64, TIn, OUT>(X, M, K, out, scales, s);
-    case 256: return launch_pack_t<256, TIn, OUT>(X, M, K, out, scales, s);
-    case 1024: return launch_pack_t<1024, TIn, OUT>(X, M, K, out, scales, s);
+    case 1: return launch_pack_t<1, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 4: return launch_pack_t<4, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 16: return launch_pack_t<16, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 64: return launch_pack_t<64, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 256: return launch_pack_t<256, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 1024: return launch_pack_t<1024, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
     default: return CONVROT_ERR_GROUP;
   }
 }
@@ -894,15 +925,22 @@ __global__ void __launch_bounds__(256) widen_kernel(const int8_t* __restrict__ s
 }  // namespace
 
 int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
-                void* out_codes, int out_kind, float* scales, cudaStream_t stream) {
+                void* out_codes, int out_kind, float* scales, cudaStream_t stream, float in_scale) {
   if (M == 0) return CONVROT_OK;
   const int k = static_cast<int>(K);
+  const float a = in_scale;
   if (x_dtype == CONVROT_F32) {
-    return out_kind == kPackI8 ? dispatch_group<float, kPackI8>(X, M, k, G, out_codes, scales, stream)
-                               : dispatch_group<float, kPackF16>(X, M, k, G, out_codes, scales, stream);
+    return out_kind == kPackI8 ? dispatch_group<float, kPackI8>(X, M, k, G, a, out_codes, scales, stream)
+                               : dispatch_group<float, kPackF16>(X, M, k, G, a, out_codes, scales, stream);
   }
-  return out_kind == kPackI8 ? dispatch_group<__half, kPackI8>(X, M, k, G, out_codes, scales, stream)
-                             : dispatch_group<__half, kPackF16>(X, M, k, G, out_codes, scales, stream);
+  return out_kind == kPackI8 ? dispatch_group<__half, kPackI8>(X, M, k, G, a, out_codes, scales, stream)
+                             : dispatch_group<__half, kPackF16>(X, M, k, G, a, out_codes, scales, stream);
+}
+
+int launch_pack_gelu(const float* X, int64_t M, int64_t K, int G, __half* out_codes, float* scales,
+                     cudaStream_t stream) {
+  if (M == 0) return CONVROT_OK;
+  return dispatch_group<float, kPackF16, kProGelu>(X, M, static_cast<int>(K), G, 1.0f, out_codes, scales, stream);
 }
 
 int read_and_clear_pack_error() {

@@ -73,6 +73,8 @@ SIGNATURES = {
     "int8_linear": (_I, [_VP, _VP, _I64, _I64, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_linear_workspace_size": (_SZ, [_I64, _I64]),
     "convrot_linear": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
+    "convrot_linear_scaled": (_I, [_VP, _I, _I64, _I64, _I, ctypes.c_float, ctypes.POINTER(convrot_weight), _I,
+                                   _VP, _SZ, _VP]),
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_weight_chunks": (_I, [_VP, _I64, _I64, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
@@ -266,6 +268,24 @@ def convrot_linear(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
     return Ys
 
 
+def convrot_linear_scaled(X: torch.Tensor, G: int, input_scale: float, q16s: Sequence[torch.Tensor],
+                          scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
+                          Ys: Optional[List[torch.Tensor]] = None, workspace=None, stream=None,
+                          kchunks=None) -> List[torch.Tensor]:
+    """convrot_linear with an input scale: X is scaled before the pack and
+    every output unscaled before its bias."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
+    ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
+    weights = make_weights(q16s, scales, biases, Ys, kchunks)
+    _check(lib().convrot_linear_scaled(_ptr(X), xd, M, K, G, float(input_scale), weights, len(q16s), _ptr(ws),
+                                       ws.numel(), _stream(stream)), "convrot_linear_scaled")
+    return Ys
+
+
 def convrot_pack_activations_f16(X: torch.Tensor, G: int, Q_x16: Optional[torch.Tensor] = None,
                                  s_x: Optional[torch.Tensor] = None, stream=None):
     """Pack X into the GEMM operand form: (Q_x16 fp16 codes [M,K], s_x f32 [M])."""
@@ -340,7 +360,7 @@ def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: 
                 stream=None) -> torch.Tensor:
     """Up linear, activation, down linear on the device. `up` and `down` are
     (q16, scale, bias, kchunk) tuples; H (optional, fp32 [M, N_up]) receives
-    the activated up output."""
+    the up linear's output before the activation."""
     xd = _xdtype(X)
     _need(X, X.dtype, "X")
     M, K = X.shape

@@ -48,6 +48,7 @@ __all__ = [
     "gemm_s32",
     "reconstruct",
     "linear",
+    "linear_scaled",
     "gelu",
 ]
 
@@ -186,6 +187,26 @@ def linear(X: np.ndarray, Qw: np.ndarray, s_w, bias, G: int) -> np.ndarray:
     """One convrot linear: pack X, integer GEMM against Q_w, reconstruct."""
     Qx, s_x = pack(X, G)
     return reconstruct(gemm_s32(Qx, Qw), s_x, s_w, bias)
+
+
+def linear_scaled(X: np.ndarray, Qw: np.ndarray, s_w, bias, G: int, input_scale: float) -> np.ndarray:
+    """One convrot linear with an input scale a ("Runtime activation
+    quantization": for input scales other than 1 the activations are scaled
+    before the convrot quantization and the output is unscaled before the
+    bias): X' = fp32(a * X), Q_x', s_x' = pack(X'), and
+    Y = (((float(A) * s_x') * s_w) / a) + b with one fp32 rounding per step.
+    """
+    a = np.float32(input_scale)
+    Xs = (np.asarray(X).astype(np.float32) * a).astype(np.float32)
+    Qx, s_x = pack(Xs, G)
+    Y = gemm_s32(Qx, Qw).astype(np.float32)
+    Y = (Y * np.asarray(s_x, np.float32)[:, None]).astype(np.float32)
+    if s_w is not None:
+        Y = (Y * np.asarray(s_w, np.float32)[None, :]).astype(np.float32)
+    Y = (Y / a).astype(np.float32)
+    if bias is not None:
+        Y = (Y + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
+    return Y
 
 
 def gelu(Y: np.ndarray) -> np.ndarray:

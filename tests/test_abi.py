@@ -138,3 +138,13 @@ def test_host_pipeline_checks(L):
     assert g(A0, ops.F32, 16, 256, 256, wts, 1, 0, None, 0, None, None, None) == ops.ERR_WORKSPACE
     assert g(A0, ops.F32, 16, 256, 256, wts, 1, -1, A3, 1 << 40, None, None, None) == ops.ERR_ARG
     assert g(A0, ops.F32, 0, 256, 256, wts, 1, 0, None, 0, None, None, None) == ops.OK
+
+
+def test_scaled_linear_rejects_bad_scales(L):
+    import ctypes
+    from int8_hadamard_rotated_gb300 import ops
+    W = ops.convrot_weight
+    ws = (W * 1)(W(A1, A2, A3, 64, A4, None))
+    f = L.convrot_linear_scaled
+    for a in (0.0, -1.0, float("inf"), float("nan")):
+        assert f(A0, ops.F32, 16, 256, 256, a, ws, 1, A5, 1 << 40, None) == ops.ERR_ARG

@@ -164,3 +164,20 @@ def test_host_pipeline_matches_device_call(ops, M, K, Ns, G, xd, chunk, streams)
     assert ops.convrot_device_status() == ops.OK
     for y, r in zip(Ys, Y_ref):
         np.testing.assert_array_equal(y.numpy(), r)
+
+
+@pytest.mark.parametrize("a", [1.0, 0.25, 3.0, 0.37])
+def test_input_scale(ops, a):
+    """convrot_linear_scaled against the oracle's scaled linear; power-of-two
+    scales give exactly the unscaled output (the oracle pins why)."""
+    w = workloads.get("unet")
+    case = workloads.make_case(w, M=333)
+    G = w.G
+    Qw, s_w, Qw16 = ops.convrot_prepare_weight(dev(case.Ws[0]), G)
+    (Y,) = ops.convrot_linear_scaled(dev(case.X), G, a, [Qw16], [s_w], [dev(case.bs[0])])
+    Y = host(Y)
+    ref = oracle.linear_scaled(case.X, host(Qw), host(s_w), case.bs[0], G, a)
+    assert_y(Y, ref)
+    if a in (1.0, 0.25):
+        (Y1,) = ops.convrot_linear(dev(case.X), G, [Qw16], [s_w], [dev(case.bs[0])])
+        np.testing.assert_array_equal(Y, host(Y1))

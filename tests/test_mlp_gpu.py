@@ -1,5 +1,6 @@
-"""convrot_mlp: up linear, GELU in the up GEMM's epilogue, repack, down linear,
-all on the device (the DiT MLP shapes), against the oracle stage by stage."""
+"""convrot_mlp: up linear, GELU applied as the down linear's pack loads the up
+output, down linear, all on the device (the DiT MLP shapes), against the
+oracle stage by stage."""
 import numpy as np
 import pytest
 import torch
@@ -25,20 +26,20 @@ def test_dit_mlp_on_device(ops, M):
     qu, su, hu, ku = prepared(ops, case.Ws[0], G)
     qd, sd, hd, kd = prepared(ops, case.Ws[1], G)
     bu, bd = dev(case.bs[0]), dev(case.bs[1])
-    H = torch.empty((M, w.Ns[0]), dtype=torch.float32, device="cuda")
-    Y = ops.convrot_mlp(dev(case.X), G, (hu, su, bu, ku), ops.ACT_GELU, G, (hd, sd, bd, kd), H=H)
-    H, Y = host(H), host(Y)
+    Y_up = torch.empty((M, w.Ns[0]), dtype=torch.float32, device="cuda")
+    Y = ops.convrot_mlp(dev(case.X), G, (hu, su, bu, ku), ops.ACT_GELU, G, (hd, sd, bd, kd), H=Y_up)
+    Y_up, Y = host(Y_up), host(Y)
     assert ops.convrot_device_status() == ops.OK
-    # stage 1: H = GELU(up linear), against the oracle with the same weight codes
+    # stage 1: the up linear, against the oracle with the same weight codes
     Qu, su_h = host(qu), host(su)
-    H_ref = oracle.gelu(oracle.linear(case.X, Qu, su_h, case.bs[0], G))
-    assert_y(H, H_ref, "H")
-    # stage 2: the down linear on the GPU's own H
+    Y_up_ref = oracle.linear(case.X, Qu, su_h, case.bs[0], G)
+    assert_y(Y_up, Y_up_ref, "Y_up")
+    # stage 2: GELU (applied as the pack loads Y_up) and the down linear, on the GPU's own Y_up
     Qd, sd_h = host(qd), host(sd)
-    assert_y(Y, oracle.linear(H, Qd, sd_h, case.bs[1], G), "down on the same H")
+    assert_y(Y, oracle.linear(oracle.gelu(Y_up), Qd, sd_h, case.bs[1], G), "GELU + down on the same Y_up")
     # the whole chain against the oracle chain (informative bar: the two
     # quantized stages compound, so the per-stage 1e-3 does not carry over)
-    assert y_rel_err(Y, oracle.linear(H_ref, Qd, sd_h, case.bs[1], G)) < 1e-2
+    assert y_rel_err(Y, oracle.linear(oracle.gelu(Y_up_ref), Qd, sd_h, case.bs[1], G)) < 1e-2
 
 
 def test_mlp_without_activation_is_two_linears(ops):

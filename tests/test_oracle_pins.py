@@ -493,3 +493,35 @@ def test_chunk_plan_reference_rule():
     p = plan(mixed)
     assert p.tolist() == [48, 16] and plan_is_safe(mixed, p)
     assert not plan_is_safe(full, np.array([32], np.int32))
+
+
+def test_linear_scaled_pins():
+    """linear_scaled against what the definition fixes: scale 1 is the plain
+    linear; a power-of-two scale commutes exactly with every fp32 step (the
+    absmax, both divisions and every product scale by the same power of two),
+    so the output equals the plain linear bit for bit; any other scale moves
+    codes by at most one step, so Y stays within the quantization error."""
+    import numpy as np
+    rng = np.random.default_rng(5)
+    M, K, N, G = 24, 256, 40, 64
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    X[3, 7] = 60.0
+    W = (rng.standard_normal((N, K)) * 0.02).astype(np.float32)
+    b = (rng.standard_normal(N) * 0.01).astype(np.float32)
+    Qw, s_w = oracle.prepare_weight(W, G)
+    Y = oracle.linear(X, Qw, s_w, b, G)
+    np.testing.assert_array_equal(oracle.linear_scaled(X, Qw, s_w, b, G, 1.0), Y)
+    for a in (0.25, 8.0, 2.0 ** -10):
+        np.testing.assert_array_equal(oracle.linear_scaled(X, Qw, s_w, b, G, a), Y)
+    for a in (3.0, 0.37, 1.7):
+        Ys = oracle.linear_scaled(X, Qw, s_w, b, G, a)
+        # one code step of X_rot is s_x; through the weights it moves Y by at most
+        # s_x * s_w * sum |Q_w| per row/column pair
+        Qx, s_x = oracle.pack(X, G)
+        bound = np.outer(s_x, s_w * np.abs(Qw.astype(np.float64)).sum(axis=1)) + 1e-6
+        assert np.all(np.abs(Ys.astype(np.float64) - Y) <= bound)
+        assert not np.array_equal(Ys, Y) or a == 1.0
+    # a forgotten unscale is caught: the output would be a times too large
+    Qx, s_x = oracle.pack((X * np.float32(3.0)).astype(np.float32), G)
+    wrong = oracle.reconstruct(oracle.gemm_s32(Qx, Qw), s_x, s_w, b)
+    assert np.max(np.abs(wrong - Y)) > 0.5 * np.max(np.abs(Y))
