@@ -285,6 +285,42 @@ int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, i
                         void* workspace, size_t workspace_bytes, void* stream,
                         void* copy_in_stream, void* copy_out_stream);
 
+/*
+ * An elementwise prologue applied to fp32 X before the convrot pack (the
+ * normalization and modulation producers the pages fuse into ConvRot:
+ * "RMSNorm -> Mul(weight) -> Modulate -> ConvRot", "Modulate -> ConvRot",
+ * scale-only modulation). In this order, each step one fp32 rounding per
+ * operation, absent parts skipped:
+ *   x <- x * (1 / sqrt(mean_k(x^2) + eps))   if rmsnorm (mean over the row)
+ *   x <- x * weight[k]                        if weight
+ *   x <- x + x * scale[k]                     if scale
+ *   x <- x + shift[k]                         if shift
+ */
+typedef struct convrot_prologue {
+  int rmsnorm;          /* nonzero: normalize each row by its RMS first */
+  float eps;            /* added to mean(x^2) before the square root */
+  const float* weight;  /* [K] per-channel multiplier, or NULL */
+  const float* scale;   /* [K] modulation scale, or NULL */
+  const float* shift;   /* [K] modulation shift, or NULL */
+} convrot_prologue;
+
+/*
+ * convrot_pack_prologue -- convrot_pack_activations of prologue(X) without
+ * writing prologue(X): X fp32 [M,K] -> Q_x int8 [M,K], s_x [M].
+ * Errors: as convrot_pack_activations; vectors must be 16-byte aligned.
+ */
+int convrot_pack_prologue(const float* X, int64_t M, int64_t K, int G,
+                          const convrot_prologue* prologue, int8_t* Q_x, float* s_x,
+                          void* stream);
+
+/*
+ * convrot_linear_prologue -- convrot_linear on prologue(X): one pack with the
+ * prologue, one grouped GEMM. Arguments and workspace as convrot_linear.
+ */
+int convrot_linear_prologue(const float* X, int64_t M, int64_t K, int G,
+                            const convrot_prologue* prologue, const convrot_weight* weights,
+                            int n_weights, void* workspace, size_t workspace_bytes, void* stream);
+
 /* Device bytes convrot_mlp needs: both packed activations and H. */
 size_t convrot_mlp_workspace_size(int64_t M, int64_t K, int64_t N_up);
 

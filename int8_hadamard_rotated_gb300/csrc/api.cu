@@ -362,6 +362,49 @@ int convrot_linear_scaled(const void* X, int x_dtype, int64_t M, int64_t K, int 
   return launch_grouped(x16, s_x, M, K, weights, n_weights, s, input_scale);
 }
 
+int convrot_pack_prologue(const float* X, int64_t M, int64_t K, int G, const convrot_prologue* pro,
+                          int8_t* Q_x, float* s_x, void* stream) {
+  if (!pro) return CONVROT_ERR_ARG;
+  if (int st = pack_checks(X, CONVROT_F32, M, K, G, Q_x, 1, s_x)) return st;
+  if (M == 0) return CONVROT_OK;
+  if ((pro->weight && !aligned16(pro->weight)) || (pro->scale && !aligned16(pro->scale)) ||
+      (pro->shift && !aligned16(pro->shift)))
+    return CONVROT_ERR_ALIGN;
+  return launch_pack_modulated(X, M, K, G, pro->weight, pro->scale, pro->shift, pro->rmsnorm != 0, pro->eps, Q_x,
+                               kPackI8, s_x, static_cast<cudaStream_t>(stream));
+}
+
+int convrot_linear_prologue(const float* X, int64_t M, int64_t K, int G, const convrot_prologue* pro,
+                            const convrot_weight* weights, int n_weights, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!pro) return CONVROT_ERR_ARG;
+  if (M < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (int st = check_weight_list(weights, n_weights)) return st;
+  if (M == 0) return CONVROT_OK;
+  if (!X) return CONVROT_ERR_ARG;
+  if (!valid_group(G, K)) return CONVROT_ERR_GROUP;
+  if (K % 16 != 0 || !aligned16(X) || (workspace && !aligned16(workspace))) return CONVROT_ERR_ALIGN;
+  if ((pro->weight && !aligned16(pro->weight)) || (pro->scale && !aligned16(pro->scale)) ||
+      (pro->shift && !aligned16(pro->shift)))
+    return CONVROT_ERR_ALIGN;
+  if (K > CONVROT_PACK_MAX_K) return CONVROT_ERR_UNSUPPORTED;
+  if (M > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  const size_t need = convrot_linear_workspace_size(M, K);
+  if (!workspace || workspace_bytes < need) return CONVROT_ERR_WORKSPACE;
+  const size_t nx = static_cast<size_t>(M) * K * 4;
+  if (overlaps(workspace, need, X, nx)) return CONVROT_ERR_ALIAS;
+  if (int st = check_weights(weights, n_weights, M, K, X, nx, workspace, need)) return st;
+  if (int st = check_device()) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __half* x16 = reinterpret_cast<__half*>(ws);
+  float* s_x = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(M) * K * 2));
+  int st = launch_pack_modulated(X, M, K, G, pro->weight, pro->scale, pro->shift, pro->rmsnorm != 0, pro->eps, x16,
+                                 kPackF16, s_x, s);
+  if (st) return st;
+  return launch_grouped(x16, s_x, M, K, weights, n_weights, s);
+}
+
 int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, void* stream) {
   if (N < 0 || K <= 0) return CONVROT_ERR_ARG;
   if (N == 0) return CONVROT_OK;

@@ -369,6 +369,13 @@ int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
 int launch_pack_gelu(const float* X, int64_t M, int64_t K, int G, __half* out_codes, float* scales,
                      cudaStream_t stream);
 
+// The pack of fp32 rows with the modulation prologue applied first: each row
+// divided by sqrt(mean(x^2) + eps) (rms != 0), times weight[k], then
+// (x + x * scale[k]) + shift[k]; null vectors are skipped.
+int launch_pack_modulated(const float* X, int64_t M, int64_t K, int G, const float* weight, const float* scale,
+                          const float* shift, int rms, float eps, void* out_codes, int out_kind, float* scales,
+                          cudaStream_t stream);
+
 // int8 codes -> fp16 codes (exact), n elements, n % 16 == 0.
 int launch_widen(const int8_t* src, __half* dst, int64_t n, cudaStream_t stream);
 

@@ -157,6 +157,15 @@ constexpr int kMaxRowsPerCta = 256;
 constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
 constexpr float kNearHalf = 0.5f - 1.0f / 32768.0f;  // 0.5 - 2^-15
 
+// Parameters of the modulation prologue (kProModulate).
+struct ModPrologue {
+  const float* weight;  // [K] per-channel multiplier after the norm, or null
+  const float* scale;   // [K] modulation scale: (x + x * scale), or null
+  const float* shift;   // [K] modulation shift: + shift, or null
+  float eps;            // RMS norm epsilon
+  int rms;              // 1: divide each row by sqrt(mean(x^2) + eps) first
+};
+
 template <typename TIn>
 struct InTraits;
 template <>
@@ -403,6 +412,7 @@ __device__ __forceinline__ void scale_unit(float (&v)[16], float a) {
 // activation, applied where its output is quantized for the down linear).
 constexpr int kProNone = 0;
 constexpr int kProGelu = 1;
+constexpr int kProModulate = 2;  // per-row RMS norm and per-channel weight / modulation (ModPrologue)
 
 template <int PRO>
 __device__ __forceinline__ void prologue_unit(float (&v)[16]) {
@@ -413,18 +423,83 @@ __device__ __forceinline__ void prologue_unit(float (&v)[16]) {
   }
 }
 
+// 1 / sqrt(sum / K + eps) of a row from its sum of squares (IEEE fp32 steps).
+__device__ __forceinline__ float rms_factor(float sumsq, int K, float eps) {
+  const float mean = __fdiv_rn(sumsq, static_cast<float>(K));
+  return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+}
+
+// The per-channel part of the modulation prologue on unit u (elements
+// 16u .. 16u+15): x * r, then * weight, then (x + x * scale) + shift, each
+// operation one fp32 rounding; absent parts are skipped.
+__device__ __forceinline__ void modulate_unit(float (&v)[16], int u, float r, bool rms, const ModPrologue& m) {
+  if (rms) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) v[p] = __fmul_rn(v[p], r);
+  }
+  if (m.weight) {
+    const float4* w4 = reinterpret_cast<const float4*>(m.weight + 16 * u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 w = __ldg(w4 + i);
+      v[4 * i] = __fmul_rn(v[4 * i], w.x);
+      v[4 * i + 1] = __fmul_rn(v[4 * i + 1], w.y);
+      v[4 * i + 2] = __fmul_rn(v[4 * i + 2], w.z);
+      v[4 * i + 3] = __fmul_rn(v[4 * i + 3], w.w);
+    }
+  }
+  if (m.scale) {
+    const float4* s4 = reinterpret_cast<const float4*>(m.scale + 16 * u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 c = __ldg(s4 + i);
+      v[4 * i] = __fadd_rn(v[4 * i], __fmul_rn(v[4 * i], c.x));
+      v[4 * i + 1] = __fadd_rn(v[4 * i + 1], __fmul_rn(v[4 * i + 1], c.y));
+      v[4 * i + 2] = __fadd_rn(v[4 * i + 2], __fmul_rn(v[4 * i + 2], c.z));
+      v[4 * i + 3] = __fadd_rn(v[4 * i + 3], __fmul_rn(v[4 * i + 3], c.w));
+    }
+  }
+  if (m.shift) {
+    const float4* h4 = reinterpret_cast<const float4*>(m.shift + 16 * u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 h = __ldg(h4 + i);
+      v[4 * i] = __fadd_rn(v[4 * i], h.x);
+      v[4 * i + 1] = __fadd_rn(v[4 * i + 1], h.y);
+      v[4 * i + 2] = __fadd_rn(v[4 * i + 2], h.z);
+      v[4 * i + 3] = __fadd_rn(v[4 * i + 3], h.w);
+    }
+  }
+}
+
+// Sum of squares of the 64 values a thread holds, reduced over the lanes of
+// its row segment.
+__device__ __forceinline__ float row_sumsq_part(const float (&v)[4][16], int segw) {
+  float ss = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int p = 0; p < 16; ++p) ss = fmaf(v[j][p], v[j][p], ss);
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1)
+    if (off < segw) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  return ss;
+}
+
 // ---- pack_kernel: the general path (per-thread cp.async) ---------------------
 
 // One CTA handles `rpc` rows with `tpr` threads each per block, persistently.
 template <int G, typename TIn, int OUT, int PRO>
 __global__ void __launch_bounds__(kMaxThreads)
 pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64_t nblocks,
-            int two_stage, float in_scale, void* __restrict__ out_codes, float* __restrict__ scales) {
+            int two_stage, float in_scale, ModPrologue mod, void* __restrict__ out_codes,
+            float* __restrict__ scales) {
   using C = Geo<G>;
   constexpr int CPU = InTraits<TIn>::kChunksPerUnit;
   constexpr int CH = 4 * CPU;  // 16-byte chunks per thread per stage
   extern __shared__ uint4 stage_buf[];  // [1 or 2][CH][blockDim.x]
   __shared__ unsigned long long s_amax[2][kMaxRowsPerCta];
+  __shared__ float s_sumsq[2][kMaxRowsPerCta];
 
   const int tid = threadIdx.x;
   const int nth = blockDim.x;
@@ -435,7 +510,10 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
   const int li = t - gi * C::kTPG;
   const bool in_cta_row = lr < rpc;
 
-  for (int i = tid; i < 2 * kMaxRowsPerCta; i += nth) (&s_amax[0][0])[i] = 0ull;
+  for (int i = tid; i < 2 * kMaxRowsPerCta; i += nth) {
+    (&s_amax[0][0])[i] = 0ull;
+    (&s_sumsq[0][0])[i] = 0.0f;
+  }
 
   const uint32_t sbase = smem_u32(stage_buf);
   auto issue = [&](int64_t blk, int stage) {
@@ -494,6 +572,22 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
       prologue_unit<PRO>(v[j]);
       if (in_scale != 1.0f) scale_unit(v[j], in_scale);
     }
+    const int slot = it & 1;
+    if (PRO == kProModulate) {
+      float r = 1.0f;
+      if (mod.rms) {
+        const float ss = row_sumsq_part(v, segw);
+        if (in_cta_row && t == 0) s_sumsq[slot ^ 1][lr] = 0.0f;  // for the next block
+        if (active && (t % segw) == 0) atomicAdd(&s_sumsq[slot][lr], ss);
+        __syncthreads();
+        r = rms_factor(s_sumsq[slot][in_cta_row ? lr : 0], K, mod.eps);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int u = in_unit_grouped<G>(gi, li, j);
+        if (active && u < units) modulate_unit(v[j], u, r, mod.rms != 0, mod);
+      }
+    }
     rotate64<G>(v, ls);
 
     unsigned abits = __float_as_uint(absmax64(v));
@@ -501,7 +595,6 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     for (int off = 1; off < 32; off <<= 1)
       if (off < segw) abits = max(abits, __shfl_xor_sync(0xffffffffu, abits, off));
     const unsigned long long tag = static_cast<unsigned long long>(it + 1) << 32;
-    const int slot = it & 1;
     if (active && (t % segw) == 0) atomicMax(&s_amax[slot][lr], tag | abits);
     __syncthreads();
     if (!active) continue;
@@ -544,6 +637,7 @@ struct PackTmaParams {
   void* out;            // codes [M, K], int8 or binary16
   float* scales;        // [M]
   float in_scale;       // input scale applied before the rotation (1 = none)
+  ModPrologue mod;      // modulation prologue (kProModulate)
   int64_t M;
   int64_t nblocks;      // ceil(M / R)
   int K;
@@ -577,7 +671,8 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   uint8_t* in_base = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.nstages) * p.stage_bytes);
   unsigned long long* s_amax = reinterpret_cast<unsigned long long*>(full + kTmaMaxStages);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_amax + 2 * p.R);
+  float* s_sumsq = reinterpret_cast<float*>(s_amax + 2 * p.R);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_sumsq + 2 * p.R);
   int* err = &g_pack_error;
 
   const int tid = threadIdx.x;
@@ -593,7 +688,10 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const int lr_read = in_cta_row ? lr : 0;  // padding threads read row 0 and store nothing
   const int S = p.nstages;
 
-  for (int i = tid; i < 2 * R; i += blockDim.x) s_amax[i] = 0ull;
+  for (int i = tid; i < 2 * R; i += blockDim.x) {
+    s_amax[i] = 0ull;
+    s_sumsq[i] = 0.0f;
+  }
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     *abort_flag = 0;
@@ -671,6 +769,20 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
       prologue_unit<PRO>(v[j]);
       if (in_scale != 1.0f) scale_unit(v[j], in_scale);
     }
+    const int slot = it & 1;
+    if (PRO == kProModulate) {
+      float r = 1.0f;
+      if (p.mod.rms) {
+        const float ss = row_sumsq_part(v, segw);
+        if (in_cta_row && t == 0) s_sumsq[(slot ^ 1) * R + lr] = 0.0f;  // for the next block
+        if (active && (t % segw) == 0) atomicAdd(&s_sumsq[slot * R + lr], ss);
+        __syncthreads();
+        r = rms_factor(s_sumsq[slot * R + lr_read], K, p.mod.eps);
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (active && u_of[j] < units) modulate_unit(v[j], u_of[j], r, p.mod.rms != 0, p.mod);
+    }
     rotate64<G>(v, ls);
 
     unsigned abits = __float_as_uint(absmax64(v));
@@ -678,7 +790,6 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
     for (int off = 1; off < 32; off <<= 1)
       if (off < segw) abits = max(abits, __shfl_xor_sync(0xffffffffu, abits, off));
     const unsigned long long tag = static_cast<unsigned long long>(it + 1) << 32;
-    const int slot = it & 1;
     if (active && (t % segw) == 0) atomicMax(&s_amax[slot * R + lr], tag | abits);
     // every thread has its inputs in registers past this barrier, so the
     // codes may overwrite the stage
@@ -763,8 +874,8 @@ int ensure_smem(Kern kern, size_t smem, size_t (&configured)[64]) {
 }
 
 template <int G, typename TIn, int OUT, int PRO>
-int launch_pack_cpasync(const void* X, int64_t M, int K, float in_scale, void* out, float* scales,
-                        cudaStream_t stream) {
+int launch_pack_cpasync(const void* X, int64_t M, int K, float in_scale, const ModPrologue& mod, void* out,
+                        float* scales, cudaStream_t stream) {
   const int tpr = (K + 63) / 64;
   int rpc = 32 / gcd_int(tpr, 32);
   int threads = tpr * rpc;
@@ -790,7 +901,7 @@ int launch_pack_cpasync(const void* X, int64_t M, int K, float in_scale, void* o
   const int64_t nblocks = (M + rpc - 1) / rpc;
   const int64_t grid = std::min<int64_t>(nblocks, static_cast<int64_t>(per_sm) * device_sm_count());
   kern<<<static_cast<unsigned>(grid), threads, smem, stream>>>(
-      static_cast<const TIn*>(X), M, K, tpr, rpc, nblocks, two_stage, in_scale, out, scales);
+      static_cast<const TIn*>(X), M, K, tpr, rpc, nblocks, two_stage, in_scale, mod, out, scales);
   return check_launch();
 }
 
@@ -825,7 +936,7 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
     rbox = 1;
   }
   const uint32_t stage_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * L * 128 + 1023) / 1024) * 1024);
-  const size_t misc = 1024 + kTmaMaxStages * 8 + 2 * static_cast<size_t>(R) * 8 + 16;
+  const size_t misc = 1024 + kTmaMaxStages * 8 + 2 * static_cast<size_t>(R) * 12 + 16;
   int S = kStages;
   while (S > 1 && misc + static_cast<size_t>(S) * stage_bytes > kSmemPerCtaMax) --S;
   smem = misc + static_cast<size_t>(S) * stage_bytes;
@@ -843,14 +954,14 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
 }
 
 template <int G, typename TIn, int OUT, int PRO>
-int launch_pack_t(const void* X, int64_t M, int K, float in_scale, void* out, float* scales,
-                  cudaStream_t stream) {
+int launch_pack_t(const void* X, int64_t M, int K, float in_scale, const ModPrologue& mod, void* out,
+                  float* scales, cudaStream_t stream) {
   PackTmaParams p;
   memset(&p, 0, sizeof(p));
   int threads = 0;
   size_t smem = 0;
   if (!plan_tma<TIn, OUT>(K, p, threads, smem))
-    return launch_pack_cpasync<G, TIn, OUT, PRO>(X, M, K, in_scale, out, scales, stream);
+    return launch_pack_cpasync<G, TIn, OUT, PRO>(X, M, K, in_scale, mod, out, scales, stream);
 
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return set_cuda_error(cudaErrorNotSupported);
@@ -870,6 +981,7 @@ int launch_pack_t(const void* X, int64_t M, int K, float in_scale, void* out, fl
   p.out = out;
   p.scales = scales;
   p.in_scale = in_scale;
+  p.mod = mod;
   p.M = M;
   p.nblocks = (M + p.R - 1) / p.R;
 
@@ -886,14 +998,15 @@ int launch_pack_t(const void* X, int64_t M, int K, float in_scale, void* out, fl
 }
 
 template <typename TIn, int OUT, int PRO = kProNone>
-int dispatch_group(const void* X, int64_t M, int K, int G, float a, void* out, float* scales, cudaStream_t s) {
+int dispatch_group(const void* X, int64_t M, int K, int G, float a, void* out, float* scales, cudaStream_t s,
+                   const ModPrologue& mod = ModPrologue{nullptr, nullptr, nullptr, 0.0f, 0}) {
   switch (G) {
-    case 1: return launch_pack_t<1, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
-    case 4: return launch_pack_t<4, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
-    case 16: return launch_pack_t<16, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
-    case 64: return launch_pack_t<64, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
-    case 256: return launch_pack_t<256, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
-    case 1024: return launch_pack_t<1024, TIn, OUT, PRO>(X, M, K, a, out, scales, s);
+    case 1: return launch_pack_t<1, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
+    case 4: return launch_pack_t<4, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
+    case 16: return launch_pack_t<16, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
+    case 64: return launch_pack_t<64, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
+    case 256: return launch_pack_t<256, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
+    case 1024: return launch_pack_t<1024, TIn, OUT, PRO>(X, M, K, a, mod, out, scales, s);
     default: return CONVROT_ERR_GROUP;
   }
 }
@@ -941,6 +1054,17 @@ int launch_pack_gelu(const float* X, int64_t M, int64_t K, int G, __half* out_co
                      cudaStream_t stream) {
   if (M == 0) return CONVROT_OK;
   return dispatch_group<float, kPackF16, kProGelu>(X, M, static_cast<int>(K), G, 1.0f, out_codes, scales, stream);
+}
+
+int launch_pack_modulated(const float* X, int64_t M, int64_t K, int G, const float* weight, const float* scale,
+                          const float* shift, int rms, float eps, void* out_codes, int out_kind, float* scales,
+                          cudaStream_t stream) {
+  if (M == 0) return CONVROT_OK;
+  const ModPrologue mod{weight, scale, shift, eps, rms};
+  const int k = static_cast<int>(K);
+  return out_kind == kPackI8
+             ? dispatch_group<float, kPackI8, kProModulate>(X, M, k, G, 1.0f, out_codes, scales, stream, mod)
+             : dispatch_group<float, kPackF16, kProModulate>(X, M, k, G, 1.0f, out_codes, scales, stream, mod);
 }
 
 int read_and_clear_pack_error() {

@@ -54,6 +54,11 @@ class ConvrotError(RuntimeError):
         self.status = status
 
 
+class convrot_prologue(ctypes.Structure):
+    _fields_ = [("rmsnorm", ctypes.c_int), ("eps", ctypes.c_float), ("weight", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p), ("shift", ctypes.c_void_p)]
+
+
 class convrot_weight(ctypes.Structure):
     _fields_ = [("q16", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("N", ctypes.c_int64),
@@ -73,6 +78,9 @@ SIGNATURES = {
     "int8_linear": (_I, [_VP, _VP, _I64, _I64, _VP, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_linear_workspace_size": (_SZ, [_I64, _I64]),
     "convrot_linear": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
+    "convrot_pack_prologue": (_I, [_VP, _I64, _I64, _I, ctypes.POINTER(convrot_prologue), _VP, _VP, _VP]),
+    "convrot_linear_prologue": (_I, [_VP, _I64, _I64, _I, ctypes.POINTER(convrot_prologue),
+                                     ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
     "convrot_linear_scaled": (_I, [_VP, _I, _I64, _I64, _I, ctypes.c_float, ctypes.POINTER(convrot_weight), _I,
                                    _VP, _SZ, _VP]),
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
@@ -283,6 +291,45 @@ def convrot_linear_scaled(X: torch.Tensor, G: int, input_scale: float, q16s: Seq
     weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear_scaled(_ptr(X), xd, M, K, G, float(input_scale), weights, len(q16s), _ptr(ws),
                                        ws.numel(), _stream(stream)), "convrot_linear_scaled")
+    return Ys
+
+
+def _prologue(rmsnorm=False, eps=1e-6, weight=None, scale=None, shift=None):
+    for name, t in (("weight", weight), ("scale", scale), ("shift", shift)):
+        if t is not None:
+            _need(t, torch.float32, name)
+    return convrot_prologue(1 if rmsnorm else 0, float(eps), _ptr(weight), _ptr(scale), _ptr(shift))
+
+
+def convrot_pack_prologue(X: torch.Tensor, G: int, rmsnorm=False, eps=1e-6, weight=None, scale=None, shift=None,
+                          Q_x=None, s_x=None, stream=None):
+    """Pack of the modulated X (RMS norm, per-channel weight, modulation) into
+    int8 codes and row scales, without materializing the modulated X."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    if Q_x is None:
+        Q_x = torch.empty((M, K), dtype=torch.int8, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float32, device=X.device)
+    pro = _prologue(rmsnorm, eps, weight, scale, shift)
+    _check(lib().convrot_pack_prologue(_ptr(X), M, K, G, ctypes.byref(pro), _ptr(Q_x), _ptr(s_x), _stream(stream)),
+           "convrot_pack_prologue")
+    return Q_x, s_x
+
+
+def convrot_linear_prologue(X: torch.Tensor, G: int, q16s, scales, biases, rmsnorm=False, eps=1e-6,
+                            weight=None, scale=None, shift=None, Ys=None, workspace=None, stream=None,
+                            kchunks=None):
+    """convrot_linear of the modulated X."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
+    ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
+    pro = _prologue(rmsnorm, eps, weight, scale, shift)
+    weights = make_weights(q16s, scales, biases, Ys, kchunks)
+    _check(lib().convrot_linear_prologue(_ptr(X), M, K, G, ctypes.byref(pro), weights, len(q16s), _ptr(ws),
+                                         ws.numel(), _stream(stream)), "convrot_linear_prologue")
     return Ys
 
 

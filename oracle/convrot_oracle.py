@@ -49,6 +49,7 @@ __all__ = [
     "reconstruct",
     "linear",
     "linear_scaled",
+    "prologue",
     "gelu",
 ]
 
@@ -207,6 +208,36 @@ def linear_scaled(X: np.ndarray, Qw: np.ndarray, s_w, bias, G: int, input_scale:
     if bias is not None:
         Y = (Y + np.asarray(bias, np.float32)[None, :]).astype(np.float32)
     return Y
+
+
+def prologue(X: np.ndarray, rmsnorm: bool = False, eps: float = 1e-6, weight=None, scale=None,
+             shift=None) -> np.ndarray:
+    """The normalization / modulation producers fused into the pack
+    ("ggml operator extensions", sd.cpp integration: Modulate computes
+    (x + x * scale) + shift with separate fp32 multiply/add rounding, and
+    RMSNorm -> Mul(weight) -> Modulate -> ConvRot is one of the fused chains).
+    In order, each operation rounded to fp32:
+      rmsnorm: r = 1 / sqrt(mean(x^2) + eps) per row (the sum of squares
+               formed in fp64 and rounded to fp32, then the mean, the sum
+               with eps, the square root and the reciprocal in fp32), x * r;
+      weight:  x * w[k];   scale: x + x * s[k];   shift: x + h[k].
+    """
+    x = np.asarray(X).astype(np.float32)
+    f32 = np.float32
+    if rmsnorm:
+        ss = (x.astype(np.float64) ** 2).sum(axis=1).astype(f32)
+        mean = (ss / f32(x.shape[1])).astype(f32)
+        d = (mean + f32(eps)).astype(f32)
+        r = (f32(1.0) / np.sqrt(d).astype(f32)).astype(f32)
+        x = (x * r[:, None]).astype(f32)
+    if weight is not None:
+        x = (x * np.asarray(weight, f32)[None, :]).astype(f32)
+    if scale is not None:
+        t = (x * np.asarray(scale, f32)[None, :]).astype(f32)
+        x = (x + t).astype(f32)
+    if shift is not None:
+        x = (x + np.asarray(shift, f32)[None, :]).astype(f32)
+    return x
 
 
 def gelu(Y: np.ndarray) -> np.ndarray:

@@ -525,3 +525,29 @@ def test_linear_scaled_pins():
     Qx, s_x = oracle.pack((X * np.float32(3.0)).astype(np.float32), G)
     wrong = oracle.reconstruct(oracle.gemm_s32(Qx, Qw), s_x, s_w, b)
     assert np.max(np.abs(wrong - Y)) > 0.5 * np.max(np.abs(Y))
+
+
+def test_prologue_pins():
+    """The modulation prologue against values fixed by its definition."""
+    import numpy as np
+    f32 = np.float32
+    # nothing requested: identity
+    X = np.random.default_rng(3).standard_normal((5, 64)).astype(f32)
+    np.testing.assert_array_equal(oracle.prologue(X), X)
+    # (x + x * scale) + shift, not x * scale + shift: 2 + 2 * 0.5 + 1 = 4
+    one = np.array([[2.0]], f32)
+    assert oracle.prologue(one, scale=np.array([0.5], f32), shift=np.array([1.0], f32))[0, 0] == 4.0
+    assert oracle.prologue(one, weight=np.array([3.0], f32))[0, 0] == 6.0
+    # RMS norm of a constant power-of-two row with eps = 0 is exactly +-1
+    c = np.full((2, 256), 4.0, f32)
+    c[1] = -0.25
+    np.testing.assert_array_equal(oracle.prologue(c, rmsnorm=True, eps=0.0), np.sign(c))
+    # RMS norm rescales each row by one factor, which the absmax quantizer
+    # divides out: the codes stay (up to rare rounding) and s_x shrinks by r
+    X = np.random.default_rng(4).standard_normal((16, 512)).astype(f32) * 7.0
+    Xn = oracle.prologue(X, rmsnorm=True, eps=1e-6)
+    Q0, s0 = oracle.pack(X, 64)
+    Q1, s1 = oracle.pack(Xn, 64)
+    assert np.count_nonzero(Q0 != Q1) <= 0.001 * Q0.size and np.abs(Q0.astype(int) - Q1).max() <= 1
+    rms = np.sqrt((X.astype(np.float64) ** 2).mean(axis=1) + 1e-6)
+    np.testing.assert_allclose(s1, s0 / rms, rtol=1e-5)

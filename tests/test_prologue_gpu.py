@@ -1,0 +1,54 @@
+"""The pack's modulation prologue (RMS norm, per-channel weight, modulation)
+on the GPU against the oracle: codes and scales of pack(prologue(X)), and the
+linear built on it."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from int8_hadamard_rotated_gb300 import workloads
+from gpu_common import dev, host
+from parity import assert_codes, assert_scales, assert_y
+
+pytestmark = pytest.mark.gpu
+
+
+def vectors(seed, K):
+    rng = workloads.rng_for(seed)
+    w = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)
+    sc = (0.2 * rng.standard_normal(K)).astype(np.float32)
+    sh = (0.05 * rng.standard_normal(K)).astype(np.float32)
+    return w, sc, sh
+
+
+@pytest.mark.parametrize("M,K,G", [(4608, 3072, 256), (37, 1280, 64), (9, 48, 4), (130, 12288, 1024)])
+@pytest.mark.parametrize("rms,use_w,use_sc,use_sh", [
+    (True, True, True, True),    # RMSNorm -> Mul(weight) -> Modulate
+    (False, False, True, True),  # Modulate
+    (False, False, True, False), # scale-only modulation
+    (True, False, False, False), # RMS norm alone
+])
+def test_pack_prologue(ops, M, K, G, rms, use_w, use_sc, use_sh):
+    rng = workloads.rng_for(M + K + G)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=30.0)
+    w, sc, sh = vectors(K, K)
+    kw = dict(rmsnorm=rms, eps=1e-6, weight=w if use_w else None, scale=sc if use_sc else None,
+              shift=sh if use_sh else None)
+    Q, s = ops.convrot_pack_prologue(dev(X), G, **{k: (dev(v) if isinstance(v, np.ndarray) else v)
+                                                   for k, v in kw.items()})
+    Qo, so = oracle.pack(oracle.prologue(X, **kw), G)
+    assert_scales(host(s), so)
+    assert_codes(host(Q), Qo)
+
+
+def test_linear_prologue(ops):
+    w = workloads.get("dit_qkv")
+    case = workloads.make_case(w, M=700)
+    g, sc, sh = vectors(1, w.K)
+    preps = [ops.convrot_prepare_weight(dev(W), w.G) for W in case.Ws[:2]]
+    Ys = ops.convrot_linear_prologue(dev(case.X), w.G, [p[2] for p in preps], [p[1] for p in preps],
+                                     [dev(b) for b in case.bs[:2]], rmsnorm=True, eps=1e-6,
+                                     weight=dev(g), scale=dev(sc), shift=dev(sh))
+    Xp = oracle.prologue(case.X, rmsnorm=True, eps=1e-6, weight=g, scale=sc, shift=sh)
+    for y, p, b in zip(Ys, preps, case.bs[:2]):
+        assert_y(host(y), oracle.linear(Xp, host(p[0]), host(p[1]), b, w.G))
