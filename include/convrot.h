@@ -165,6 +165,22 @@ typedef struct convrot_weight {
                             or NULL (chunks of 1024 products) */
 } convrot_weight;
 
+/*
+ * convrot_w4_expand -- weights of the packed INT4 convrot format ("Packed
+ * INT4 convrot", convrot_w4a4: signed 4-bit weights, low nibble first, with
+ * an F32 per-output weight scale; activations use the INT8 convrot pack) into
+ * the codes the GEMM reads. Element 2j of a row is the low nibble of byte j,
+ * element 2j+1 the high nibble, each a two's-complement value in [-8, 7].
+ * A W4A4 linear is then convrot_linear with these codes and the checkpoint's
+ * weight scale.
+ *   Q_w4   [N, K/2] packed bytes (input).
+ *   Q_w    [N,K] int8 codes (output, may be NULL; feeds convrot_weight_chunks).
+ *   Q_w16  [N,K] binary16 codes (output, may be NULL). Not both NULL.
+ * Errors: ERR_ARG, ERR_ALIGN (K % 16, 16-byte arrays), ERR_ALIAS, ERR_CUDA.
+ */
+int convrot_w4_expand(const uint8_t* Q_w4, int64_t N, int64_t K, int8_t* Q_w,
+                      uint16_t* Q_w16, void* stream);
+
 /* Weight rows per entry of a chunk plan. */
 #define CONVROT_CHUNK_ROWS 128
 

@@ -405,6 +405,21 @@ int convrot_linear_prologue(const float* X, int64_t M, int64_t K, int G, const c
   return launch_grouped(x16, s_x, M, K, weights, n_weights, s);
 }
 
+int convrot_w4_expand(const uint8_t* Q_w4, int64_t N, int64_t K, int8_t* Q_w, uint16_t* Q_w16, void* stream) {
+  if (N < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (N == 0) return CONVROT_OK;
+  if (!Q_w4 || (!Q_w && !Q_w16)) return CONVROT_ERR_ARG;
+  if (K % 16 != 0 || !aligned16(Q_w4) || (Q_w && !aligned16(Q_w)) || (Q_w16 && !aligned16(Q_w16)))
+    return CONVROT_ERR_ALIGN;
+  if (N > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  const size_t n = static_cast<size_t>(N) * K;
+  if (overlaps(Q_w4, n / 2, Q_w, n) || overlaps(Q_w4, n / 2, Q_w16, n * 2) || overlaps(Q_w, n, Q_w16, n * 2))
+    return CONVROT_ERR_ALIAS;
+  if (int st = check_device()) return st;
+  return launch_w4_expand(Q_w4, static_cast<int64_t>(n), Q_w, reinterpret_cast<__half*>(Q_w16),
+                          static_cast<cudaStream_t>(stream));
+}
+
 int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, void* stream) {
   if (N < 0 || K <= 0) return CONVROT_ERR_ARG;
   if (N == 0) return CONVROT_OK;

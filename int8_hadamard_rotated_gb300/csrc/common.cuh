@@ -376,6 +376,10 @@ int launch_pack_modulated(const float* X, int64_t M, int64_t K, int G, const flo
                           const float* shift, int rms, float eps, void* out_codes, int out_kind, float* scales,
                           cudaStream_t stream);
 
+// Packed signed 4-bit codes (two per byte, low nibble first) -> int8 and/or
+// binary16 codes, n elements, n % 16 == 0; either output may be null.
+int launch_w4_expand(const uint8_t* src, int64_t n, int8_t* q8, __half* q16, cudaStream_t stream);
+
 // int8 codes -> fp16 codes (exact), n elements, n % 16 == 0.
 int launch_widen(const int8_t* src, __half* dst, int64_t n, cudaStream_t stream);
 

@@ -1035,7 +1035,51 @@ __global__ void __launch_bounds__(256) widen_kernel(const int8_t* __restrict__ s
   d[1] = make_uint4(h[4], h[5], h[6], h[7]);
 }
 
+// Packed signed 4-bit weights ("Packed INT4 convrot": low nibble first) to
+// int8 and/or binary16 codes; 16 values (8 bytes) per thread.
+__global__ void __launch_bounds__(256) w4_expand_kernel(const uint8_t* __restrict__ src, int64_t n8,
+                                                        int8_t* __restrict__ q8, __half* __restrict__ q16) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= n8) return;
+  const uint2 a = __ldcs(reinterpret_cast<const uint2*>(src) + i);
+  const uint32_t w[2] = {a.x, a.y};
+  int v[16];
+#pragma unroll
+  for (int k = 0; k < 2; ++k)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t byte = (w[k] >> (8 * b)) & 0xffu;
+      const int lo = static_cast<int>(byte & 0xfu), hi = static_cast<int>(byte >> 4);
+      v[8 * k + 2 * b] = lo >= 8 ? lo - 16 : lo;       // element 2j: low nibble
+      v[8 * k + 2 * b + 1] = hi >= 8 ? hi - 16 : hi;   // element 2j+1: high nibble
+    }
+  if (q8) {
+    uint32_t o[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      o[k] = (static_cast<uint32_t>(v[4 * k] & 0xff)) | (static_cast<uint32_t>(v[4 * k + 1] & 0xff) << 8) |
+             (static_cast<uint32_t>(v[4 * k + 2] & 0xff) << 16) | (static_cast<uint32_t>(v[4 * k + 3] & 0xff) << 24);
+    reinterpret_cast<uint4*>(q8)[i] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+  if (q16) {
+    uint32_t h[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) h[k] = pack2_f16(v[2 * k], v[2 * k + 1]);
+    uint4* d = reinterpret_cast<uint4*>(q16) + 2 * i;
+    d[0] = make_uint4(h[0], h[1], h[2], h[3]);
+    d[1] = make_uint4(h[4], h[5], h[6], h[7]);
+  }
+}
+
 }  // namespace
+
+int launch_w4_expand(const uint8_t* src, int64_t n, int8_t* q8, __half* q16, cudaStream_t stream) {
+  if (n == 0) return CONVROT_OK;
+  const int64_t n8 = n / 16;  // 16 values = 8 packed bytes per thread
+  const int64_t blocks = (n8 + 255) / 256;
+  w4_expand_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(src, n8, q8, q16);
+  return check_launch();
+}
 
 int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                 void* out_codes, int out_kind, float* scales, cudaStream_t stream, float in_scale) {

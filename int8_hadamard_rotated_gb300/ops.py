@@ -85,6 +85,7 @@ SIGNATURES = {
                                    _VP, _SZ, _VP]),
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_weight_chunks": (_I, [_VP, _I64, _I64, _VP, _VP]),
+    "convrot_w4_expand": (_I, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
     "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
@@ -229,6 +230,19 @@ def convrot_weight_chunks(Q_w: torch.Tensor, kchunk: Optional[torch.Tensor] = No
         kchunk = torch.empty(((N + CHUNK_ROWS - 1) // CHUNK_ROWS,), dtype=torch.int32, device=Q_w.device)
     _check(lib().convrot_weight_chunks(_ptr(Q_w), N, K, _ptr(kchunk), _stream(stream)), "convrot_weight_chunks")
     return kchunk
+
+
+def convrot_w4_expand(Q_w4: torch.Tensor, K: int, with_int8: bool = True, stream=None):
+    """Packed signed 4-bit weights [N, K/2] (uint8, low nibble first) ->
+    (int8 codes or None, binary16 codes) [N, K]."""
+    _need(Q_w4, torch.uint8, "Q_w4")
+    N = Q_w4.shape[0]
+    if Q_w4.shape[1] * 2 != K:
+        raise ValueError("Q_w4 must be [N, K/2]")
+    q8 = torch.empty((N, K), dtype=torch.int8, device=Q_w4.device) if with_int8 else None
+    q16 = torch.empty((N, K), dtype=torch.float16, device=Q_w4.device)
+    _check(lib().convrot_w4_expand(_ptr(Q_w4), N, K, _ptr(q8), _ptr(q16), _stream(stream)), "convrot_w4_expand")
+    return q8, q16
 
 
 def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None, kchunk=None) -> torch.Tensor:

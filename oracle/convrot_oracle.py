@@ -50,6 +50,7 @@ __all__ = [
     "linear",
     "linear_scaled",
     "prologue",
+    "unpack_w4",
     "gelu",
 ]
 
@@ -238,6 +239,22 @@ def prologue(X: np.ndarray, rmsnorm: bool = False, eps: float = 1e-6, weight=Non
     if shift is not None:
         x = (x + np.asarray(shift, f32)[None, :]).astype(f32)
     return x
+
+
+def unpack_w4(packed: np.ndarray) -> np.ndarray:
+    """Weights of the packed INT4 convrot format ("INT8 Convrot Safetensors",
+    Packed INT4 convrot: signed 4-bit values, low nibble first): byte j of a
+    row holds element 2j in its low and element 2j+1 in its high four bits,
+    each a two's-complement value in [-8, 7]. Returns int8 [N, 2 * bytes]."""
+    b = np.asarray(packed, dtype=np.uint8).astype(np.int16)
+    lo = b & 0xF
+    hi = b >> 4
+    lo = np.where(lo >= 8, lo - 16, lo)
+    hi = np.where(hi >= 8, hi - 16, hi)
+    out = np.empty((b.shape[0], 2 * b.shape[1]), dtype=np.int8)
+    out[:, 0::2] = lo
+    out[:, 1::2] = hi
+    return out
 
 
 def gelu(Y: np.ndarray) -> np.ndarray:

@@ -551,3 +551,16 @@ def test_prologue_pins():
     assert np.count_nonzero(Q0 != Q1) <= 0.001 * Q0.size and np.abs(Q0.astype(int) - Q1).max() <= 1
     rms = np.sqrt((X.astype(np.float64) ** 2).mean(axis=1) + 1e-6)
     np.testing.assert_allclose(s1, s0 / rms, rtol=1e-5)
+
+
+def test_unpack_w4_pins():
+    """Packed INT4 layout: low nibble first, two's complement in [-8, 7]."""
+    import numpy as np
+    packed = np.array([[0x8F, 0x71, 0x00, 0xF8]], np.uint8)
+    assert oracle.unpack_w4(packed).tolist() == [[-1, -8, 1, 7, 0, 0, -8, -1]]
+    # every byte value round-trips through its two nibbles
+    allb = np.arange(256, dtype=np.uint8)[None, :]
+    q = oracle.unpack_w4(allb).astype(np.int16)
+    back = ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
+    np.testing.assert_array_equal(back, allb)
+    assert q.min() == -8 and q.max() == 7
