@@ -66,7 +66,12 @@ constexpr int RASTER_BANDS = 8;       // activation bands per raster group
 static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
 
-template <int CG, int BN_>
+// Y staging for tensor-map stores: per epilogue warpgroup one buffer of
+// Y_ROWS activation rows x 128 output features (fp32).
+constexpr int Y_ROWS = 16;
+constexpr int Y_HALF_BYTES = Y_ROWS * CTA_M * 4;
+
+template <int CG, int BN_, bool YTMA = false>
 struct Geom {
   static constexpr int BN = BN_;                      // activation rows per tile (MMA N)
   static constexpr int COLS = BN / 2;                 // columns per epilogue thread (two warpgroups)
@@ -78,21 +83,23 @@ struct Geom {
   static constexpr int STAGES = (196 * 1024) / STAGE_BYTES;  // 4 (CG 1), 6-8 (pairs)
   static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN);
   // shared-memory layout (after aligning the base to 1024 B)
-  static constexpr int SMEM_BARS = STAGES * STAGE_BYTES;  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int SMEM_YOUT = STAGES * STAGE_BYTES;                  // [2][Y_ROWS][128] fp32 (YTMA)
+  static constexpr int SMEM_BARS = SMEM_YOUT + (YTMA ? 2 * Y_HALF_BYTES : 0);  // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
   static constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;  // tmem base (u32), abort flag (int)
   // slack for the 1024-B alignment, and (pairs) one more half tile so that
   // every operand read of the last stage stays inside the allocation
-  static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024 + (CG == 2 ? X_BYTES : 0);
+  static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;
 };
-static_assert(Geom<1, 256>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 256>::SMEM_ALLOC <= 227 * 1024 &&
-                  Geom<2, 192>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 128>::SMEM_ALLOC <= 227 * 1024,
+static_assert(Geom<1, 256>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 256, true>::SMEM_ALLOC <= 227 * 1024 &&
+                  Geom<2, 192, true>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 128, true>::SMEM_ALLOC <= 227 * 1024,
               "shared memory");
 static_assert(2 * 256 <= TMEM_COLS, "two accumulators fit in TMEM");
 
 struct GemmParams {
   CUtensorMap tmap_x;              // activation codes, fp16 [M, K], box X_ROWS x 64
   CUtensorMap tmap_w[MAX_LIN];     // weight codes, fp16 [N_j, K], box 128 x 64
+  CUtensorMap tmap_y[MAX_LIN];     // fp32 Y_j [M, N_j], box 128 x Y_ROWS (YTMA kernels)
   const float* s_w[MAX_LIN];
   const float* bias[MAX_LIN];
   const int32_t* kchunk[MAX_LIN];  // exact-chunk plan per 128 weight rows, or null
@@ -154,10 +161,12 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
 
 // UNSCALE: the variant for linears with an input scale other than 1 (the IEEE
 // division stays out of the common kernel's unrolled epilogue).
-template <int CG, int BN_, bool UNSCALE>
+// YTMA: Y leaves through shared memory and tensor-map stores (16 rows x 128
+// features per store) instead of per-thread global stores.
+template <int CG, int BN_, bool UNSCALE, bool YTMA>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Gm = Geom<CG, BN_>;
+  using Gm = Geom<CG, BN_, YTMA>;
   constexpr int BN = Gm::BN;
   constexpr int COLS_PER_THREAD = Gm::COLS;
   constexpr int STAGES = Gm::STAGES;
@@ -337,6 +346,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         }
         ++chunk_iter;
       }
+      // the warpgroup leaves together (its stores use a barrier of its own)
+      if (YTMA) ok = named_bar_and(1 + half, 4 * 32, ok);
       if (!ok) break;
       const int N = p.N[c.lin];
       const int o = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
@@ -365,21 +376,54 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const float sw = (o_ok && sw_ptr) ? __ldg(sw_ptr + o) : 1.0f;
         const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
         const float in_scale = UNSCALE ? p.in_scale[c.lin] : 1.0f;
+        if (YTMA) {
+          // Y_ROWS rows at a time through this warpgroup's staging buffer and
+          // one tensor-map store (rows past M and features past N are not
+          // written by the store)
+          float* sy = reinterpret_cast<float*>(smem + Gm::SMEM_YOUT + half * Y_HALF_BYTES);
+          const bool store_leader = (quarter == 0 && lane == 0);
+          const int col = 32 * quarter + lane;
+          const int o_base = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
 #pragma unroll
-        for (int i = 0; i < COLS_PER_THREAD; ++i) {
-          const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
-          const int r = r0 + i;
-          if (o_ok && r < p.M) {
-            // float(A) * s_x * s_w + b, one rounding per operation, in that order
-            float y = __fmul_rn(__int2float_rn(acc[i]), sx);
-            if (sw_ptr) y = __fmul_rn(y, sw);
-            if (UNSCALE) y = __fdiv_rn(y, in_scale);  // unscale before the bias
-            if (b_ptr) y = __fadd_rn(y, bb);
-            st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
+          for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
+            if (store_leader) bulk_wait_read<0>();  // the previous store has read the buffer
+            named_bar_sync(1 + half, 4 * 32);
+#pragma unroll
+            for (int i = 0; i < Y_ROWS; ++i) {
+              const int idx = sub * Y_ROWS + i;
+              const float sx = __shfl_sync(0xffffffffu, sxv[idx >> 5], idx & 31);
+              // float(A) * s_x * s_w + b, one rounding per operation, in that order
+              float y = __fmul_rn(__int2float_rn(acc[idx]), sx);
+              if (sw_ptr) y = __fmul_rn(y, sw);
+              if (b_ptr) y = __fadd_rn(y, bb);
+              sy[i * CTA_M + col] = y;
+            }
+            fence_proxy_async_smem();
+            named_bar_sync(1 + half, 4 * 32);
+            if (store_leader && o_base < N && r0 + sub * Y_ROWS < p.M) {
+              tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
+              bulk_commit();
+            }
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < COLS_PER_THREAD; ++i) {
+            const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
+            const int r = r0 + i;
+            if (o_ok && r < p.M) {
+              // float(A) * s_x * s_w + b, one rounding per operation, in that order
+              float y = __fmul_rn(__int2float_rn(acc[i]), sx);
+              if (sw_ptr) y = __fmul_rn(y, sw);
+              if (UNSCALE) y = __fdiv_rn(y, in_scale);  // unscale before the bias
+              if (b_ptr) y = __fadd_rn(y, bb);
+              st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
+            }
           }
         }
       }
     }
+    // the last tensor-map stores complete before the CTA releases its shared memory
+    if (YTMA && (warp & 3) == 0 && lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -406,6 +450,21 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_cuda_error(cudaErrorInvalidValue);
+  return CONVROT_OK;
+}
+
+// fp32 Y [rows, cols] row-major (cols % 4 == 0), box 128 features x Y_ROWS rows, no swizzle.
+int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return set_cuda_error(cudaErrorNotSupported);
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(CTA_M), static_cast<cuuint32_t>(Y_ROWS)};
+  const cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return set_cuda_error(cudaErrorInvalidValue);
   return CONVROT_OK;
 }
@@ -446,7 +505,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
 }
 
 // Raise the kernel's shared-memory limit once per device.
-template <int CG, int BN, bool UNSCALE>
+template <int CG, int BN, bool UNSCALE, bool YTMA>
 int configure_kernel() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -455,8 +514,8 @@ int configure_kernel() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Geom<CG, BN>::SMEM_ALLOC);
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE, YTMA>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Geom<CG, BN, YTMA>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
   }
@@ -490,9 +549,9 @@ int max_pairs() {
   std::lock_guard<std::mutex> lock(mu);
   if (!known[dev]) {
     cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = pair_config(device_sm_count(), Geom<2, BN>::SMEM_ALLOC, nullptr, attr);
+    cudaLaunchConfig_t cfg = pair_config(device_sm_count(), Geom<2, BN, true>::SMEM_ALLOC, nullptr, attr);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false, true>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the sticky launch-query error
       n = 0;
     }
@@ -502,17 +561,20 @@ int max_pairs() {
   return cached[dev];
 }
 
-template <int BN, bool UNSCALE>
+template <int BN, bool UNSCALE, bool YTMA>
 int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
                  bool raw_s32, int pairs, cudaStream_t stream) {
   GemmParams p;
   if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
+  if (YTMA)
+    for (int j = 0; j < n_lin; ++j)
+      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
   cudaLaunchAttribute attr[1];
   const cudaLaunchConfig_t cfg =
-      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN>::SMEM_ALLOC, stream, attr);
-  if (int st = configure_kernel<2, BN, UNSCALE>()) return st;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE>, p);
+      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr);
+  if (int st = configure_kernel<2, BN, UNSCALE, YTMA>()) return st;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE, YTMA>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
   return check_launch();
 }
@@ -614,33 +676,42 @@ int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs) {
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream) {
   if (M == 0) return CONVROT_OK;
-  bool unscale = false;
-  for (int j = 0; j < n_lin; ++j) unscale |= (lins[j].in_scale != 1.0f);
-  if (int st = configure_kernel<2, 256, false>()) return st;
-  if (int st = configure_kernel<2, 192, false>()) return st;
-  if (int st = configure_kernel<2, 128, false>()) return st;
+  bool unscale = false, ytma = !raw_s32;
+  for (int j = 0; j < n_lin; ++j) {
+    unscale |= (lins[j].in_scale != 1.0f);
+    ytma &= (lins[j].N % 4 == 0);  // tensor-map rows must be multiples of 16 bytes
+  }
+  ytma &= !unscale;
+  if (int st = configure_kernel<2, 256, false, true>()) return st;
+  if (int st = configure_kernel<2, 192, false, true>()) return st;
+  if (int st = configure_kernel<2, 128, false, true>()) return st;
   const int pairs = std::min(max_pairs<256>(), std::min(max_pairs<192>(), max_pairs<128>()));
   if (pairs > 0) {
     const int bn = pick_tile_rows(M, lins, n_lin, pairs);
-    if (unscale) {
-      if (bn == 128) return launch_pairs<128, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      if (bn == 192) return launch_pairs<192, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      return launch_pairs<256, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    if (ytma) {
+      if (bn == 128) return launch_pairs<128, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      if (bn == 192) return launch_pairs<192, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      return launch_pairs<256, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
     }
-    if (bn == 128) return launch_pairs<128, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-    if (bn == 192) return launch_pairs<192, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-    return launch_pairs<256, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    if (unscale) {
+      if (bn == 128) return launch_pairs<128, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      if (bn == 192) return launch_pairs<192, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      return launch_pairs<256, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    }
+    if (bn == 128) return launch_pairs<128, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    if (bn == 192) return launch_pairs<192, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    return launch_pairs<256, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
   }
   GemmParams p;
   if (int st = fill_params<1, 256>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
   const int grid = std::min(p.total_tiles, device_sm_count());
   if (unscale) {
-    if (int st = configure_kernel<1, 256, true>()) return st;
-    convrot_gemm_kernel<1, 256, true><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
+    if (int st = configure_kernel<1, 256, true, false>()) return st;
+    convrot_gemm_kernel<1, 256, true, false><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
   } else {
-    if (int st = configure_kernel<1, 256, false>()) return st;
-    convrot_gemm_kernel<1, 256, false><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
+    if (int st = configure_kernel<1, 256, false, false>()) return st;
+    convrot_gemm_kernel<1, 256, false, false><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
   }
   return check_launch();
 }
