@@ -131,6 +131,16 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, const void* smem_
                ::"l"(tmap), "r"(smem_u32(smem_src)), "r"(x), "r"(y) : "memory");
 }
 
+// Programmatic dependent launch: let the next kernel in the stream start
+// launching (its own prologue), and, in that kernel, wait until every kernel
+// it depends on has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Barrier over `nthreads` threads (a multiple of 32) using hardware barrier `id` (1..15).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");

@@ -220,6 +220,10 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   if (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_base_smem;
+  // Launched as a programmatic dependent of the kernel before it (the pack):
+  // everything above overlapped that kernel; nothing below may read or write
+  // global memory before it has completed.
+  pdl_wait_prerequisites();
 
   if (warp == PRODUCER_WARP) {
     if (lane == 0) {
@@ -522,18 +526,24 @@ int configure_kernel() {
   return CONVROT_OK;
 }
 
-cudaLaunchConfig_t pair_config(int n_pairs, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr) {
+// Launch configuration of the CTA-pair kernel: clusters of two and, when
+// `pdl`, programmatic serialization after the previous kernel in the stream
+// (the kernel waits for it with griddepcontrol.wait after its own setup).
+cudaLaunchConfig_t pair_config(int n_pairs, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr,
+                               bool pdl = false) {
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * n_pairs, 1, 1);
   cfg.blockDim = dim3(THREADS, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cfg;
 }
 
@@ -548,7 +558,7 @@ int max_pairs() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
   std::lock_guard<std::mutex> lock(mu);
   if (!known[dev]) {
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     cudaLaunchConfig_t cfg = pair_config(device_sm_count(), Geom<2, BN, true>::SMEM_ALLOC, nullptr, attr);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false, true>, &cfg) != cudaSuccess) {
@@ -570,9 +580,9 @@ int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, cons
   if (YTMA)
     for (int j = 0; j < n_lin; ++j)
       if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg =
-      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr);
+      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true);
   if (int st = configure_kernel<2, BN, UNSCALE, YTMA>()) return st;
   cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE, YTMA>, p);
   if (e != cudaSuccess) return set_cuda_error(e);

@@ -510,6 +510,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
   const int li = t - gi * C::kTPG;
   const bool in_cta_row = lr < rpc;
 
+  pdl_launch_dependents();  // the next kernel may set itself up; it waits for this one before reading
   for (int i = tid; i < 2 * kMaxRowsPerCta; i += nth) {
     (&s_amax[0][0])[i] = 0ull;
     (&s_sumsq[0][0])[i] = 0.0f;
@@ -688,6 +689,7 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const int lr_read = in_cta_row ? lr : 0;  // padding threads read row 0 and store nothing
   const int S = p.nstages;
 
+  pdl_launch_dependents();  // the next kernel may set itself up; it waits for this one before reading
   for (int i = tid; i < 2 * R; i += blockDim.x) {
     s_amax[i] = 0ull;
     s_sumsq[i] = 0.0f;
