@@ -209,6 +209,7 @@ def run_gpu(args, rank, world, local_rank):
     Qx16 = torch.empty((w.M, w.K), dtype=torch.float16, device=dev)
     s_x = torch.empty((w.M,), dtype=torch.float32, device=dev)
     wdesc = ops.make_weights(q16s, scales, biases, Ys, plans)
+    sync_ws = torch.empty((ops.GEMM_SYNC_BYTES,), dtype=torch.uint8, device=dev)  # GEMM hand-over words
     L = ops.lib()
     sp = stream.cuda_stream
     flush = torch.empty((L2_FLUSH_BYTES,), dtype=torch.uint8, device=dev)
@@ -221,7 +222,8 @@ def run_gpu(args, rank, world, local_rank):
         return st
 
     def gemm():
-        st = L.convrot_linear_packed(Qx16.data_ptr(), s_x.data_ptr(), w.M, w.K, wdesc, len(q16s), sp)
+        st = L.convrot_linear_packed(Qx16.data_ptr(), s_x.data_ptr(), w.M, w.K, wdesc, len(q16s),
+                                     sync_ws.data_ptr(), ops.GEMM_SYNC_BYTES, sp)
         if st:
             raise ops.ConvrotError(st, "gemm")
 

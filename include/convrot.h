@@ -132,8 +132,22 @@ int convrot_pack_activations(const void* X, int x_dtype, int64_t M, int64_t K,
                              int G, int8_t* Q_x, float* s_x, void* stream);
 
 /*
+ * Bytes of the GEMM's hand-over words, part of every workspace below. When the
+ * last wave of output tiles would leave CTA pairs idle, the GEMM splits the
+ * remaining tiles by K over all pairs; a pair that ends inside a tile passes
+ * its int32 partial sums (stored in that tile's output) to the pair that
+ * finishes it, and these words say when they are ready (one 8-byte word per
+ * CTA, up to 256 CTA pairs). Their content between calls needs no
+ * initialization: a call writes a value unique to it and zeroes what it
+ * consumed. A workspace must not be used by two calls that run at the same
+ * time.
+ */
+#define CONVROT_GEMM_SYNC_BYTES 4096
+
+/*
  * int8_linear_workspace_size -- device bytes int8_linear needs: room to widen
- * Q_x (and Q_w when Q_w16 is not given) to binary16 codes.
+ * Q_x (and Q_w when Q_w16 is not given) to binary16 codes, and the GEMM's
+ * hand-over words (CONVROT_GEMM_SYNC_BYTES).
  */
 size_t int8_linear_workspace_size(int64_t M, int64_t N, int64_t K,
                                   int have_q_w16);
@@ -201,7 +215,8 @@ int convrot_w4_expand(const uint8_t* Q_w4, int64_t N, int64_t K, int8_t* Q_w,
 int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk,
                           void* stream);
 
-/* Device bytes convrot_linear needs for the shared packed activation. */
+/* Device bytes convrot_linear needs: the shared packed activation and the
+ * GEMM's hand-over words (CONVROT_GEMM_SYNC_BYTES). */
 size_t convrot_linear_workspace_size(int64_t M, int64_t K);
 
 /*
@@ -262,17 +277,24 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
 /*
  * convrot_linear_packed -- the grouped GEMM of convrot_linear on an activation
  * packed by convrot_pack_activations_f16: every
- * Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j. Needs no workspace.
+ * Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j.
  *   Q_x16 [M,K] binary16 codes, s_x [M] fp32; weights as convrot_linear.
- * Errors: ERR_ARG, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS, ERR_UNSUPPORTED, ERR_CUDA.
+ *   workspace  NULL, or CONVROT_GEMM_SYNC_BYTES bytes of device scratch
+ *              (16-byte aligned) for the GEMM's hand-over words; without it
+ *              the GEMM takes whole tiles only (same results, a less even
+ *              last wave).
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_OVERFLOW, ERR_ALIAS, ERR_WORKSPACE (workspace
+ *         given but smaller than CONVROT_GEMM_SYNC_BYTES), ERR_UNSUPPORTED, ERR_CUDA.
  */
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
-                          const convrot_weight* weights, int n_weights, void* stream);
+                          const convrot_weight* weights, int n_weights,
+                          void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * convrot_linear_host_workspace_size -- device bytes convrot_linear_host needs:
  * two sets of chunk buffers (input rows, binary16 codes, row scales and the
- * output rows of all linears, n_total = sum of their N). chunk_rows = 0 picks
+ * output rows of all linears, n_total = sum of their N) and the GEMM's
+ * hand-over words (CONVROT_GEMM_SYNC_BYTES). chunk_rows = 0 picks
  * the library default (768 rows). Returns 0 for invalid arguments.
  */
 size_t convrot_linear_host_workspace_size(int64_t M, int64_t K, int x_dtype,
@@ -337,7 +359,8 @@ int convrot_linear_prologue(const float* X, int64_t M, int64_t K, int G,
                             const convrot_prologue* prologue, const convrot_weight* weights,
                             int n_weights, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Device bytes convrot_mlp needs: both packed activations and H. */
+/* Device bytes convrot_mlp needs: both packed activations, H and the GEMM's
+ * hand-over words (CONVROT_GEMM_SYNC_BYTES). */
 size_t convrot_mlp_workspace_size(int64_t M, int64_t K, int64_t N_up);
 
 /*

@@ -140,12 +140,13 @@ size_t int8_linear_workspace_size(int64_t M, int64_t N, int64_t K, int have_q_w1
   if (M < 0 || N < 0 || K < 0) return 0;
   size_t b = round256(static_cast<size_t>(M) * K * 2);
   if (!have_q_w16) b += round256(static_cast<size_t>(N) * K * 2);
-  return b;
+  return b + CONVROT_GEMM_SYNC_BYTES;
 }
 
 size_t convrot_linear_workspace_size(int64_t M, int64_t K) {
   if (M < 0 || K < 0) return 0;
-  return round256(static_cast<size_t>(M) * K * 2) + round256(static_cast<size_t>(M) * 4);
+  return round256(static_cast<size_t>(M) * K * 2) + round256(static_cast<size_t>(M) * 4) +
+         CONVROT_GEMM_SYNC_BYTES;
 }
 
 }  // extern "C"
@@ -193,7 +194,7 @@ int int8_gemm_common(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
     w16 = wtmp;
   }
   GemmLinear lin{w16, s_w, bias, out, N, kchunk};
-  return launch_gemm(x16, s_x, M, K, &lin, 1, raw, s);
+  return launch_gemm(x16, s_x, M, K, &lin, 1, raw, s, sync_at(ws + need - CONVROT_GEMM_SYNC_BYTES));
 }
 
 }  // namespace
@@ -259,7 +260,8 @@ int check_weight_list(const convrot_weight* weights, int n_weights) {
 }
 
 int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale) {
+                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale,
+                   GemmSync sync) {
   GemmLinear lins[CONVROT_MAX_LINEARS];
   int n = 0;
   for (int j = 0; j < n_weights; ++j) {
@@ -268,7 +270,7 @@ int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
     lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N, w.kchunk, in_scale};
   }
   if (n == 0) return CONVROT_OK;
-  return launch_gemm(x16, s_x, M, K, lins, n, false, s);
+  return launch_gemm(x16, s_x, M, K, lins, n, false, s, sync);
 }
 
 }  // namespace convrot
@@ -304,20 +306,36 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
 }
 
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
-                          const convrot_weight* weights, int n_weights, void* stream) {
+                          const convrot_weight* weights, int n_weights,
+                          void* workspace, size_t workspace_bytes, void* stream) {
   if (M < 0 || K <= 0) return CONVROT_ERR_ARG;
   if (int st = check_weight_list(weights, n_weights)) return st;
   if (M == 0) return CONVROT_OK;
   if (!Q_x16 || !s_x) return CONVROT_ERR_ARG;
-  if (K % 16 != 0 || !aligned16(Q_x16) || !aligned16(s_x)) return CONVROT_ERR_ALIGN;
+  if (K % 16 != 0 || !aligned16(Q_x16) || !aligned16(s_x) || (workspace && !aligned16(workspace)))
+    return CONVROT_ERR_ALIGN;
+  if (workspace && workspace_bytes < CONVROT_GEMM_SYNC_BYTES) return CONVROT_ERR_WORKSPACE;
   if (K > CONVROT_MAX_K) return CONVROT_ERR_OVERFLOW;
   if (M > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  if (workspace && (overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, Q_x16, static_cast<size_t>(M) * K * 2) ||
+                    overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, s_x, static_cast<size_t>(M) * 4)))
+    return CONVROT_ERR_ALIAS;
   if (int st = check_weights(weights, n_weights, M, K, Q_x16, static_cast<size_t>(M) * K * 2, s_x,
                              static_cast<size_t>(M) * 4))
     return st;
+  if (workspace)
+    for (int j = 0; j < n_weights; ++j) {
+      const convrot_weight& w = weights[j];
+      if (w.N == 0) continue;
+      if (overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.Y, static_cast<size_t>(M) * w.N * 4) ||
+          overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.q16, static_cast<size_t>(w.N) * K * 2) ||
+          (w.scale && overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.scale, w.N * 4)) ||
+          (w.bias && overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.bias, w.N * 4)))
+        return CONVROT_ERR_ALIAS;
+    }
   if (int st = check_device()) return st;
   return launch_grouped(reinterpret_cast<const __half*>(Q_x16), s_x, M, K, weights, n_weights,
-                        static_cast<cudaStream_t>(stream));
+                        static_cast<cudaStream_t>(stream), 1.0f, workspace ? sync_at(workspace) : GemmSync());
 }
 
 int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
@@ -359,7 +377,8 @@ int convrot_linear_scaled(const void* X, int x_dtype, int64_t M, int64_t K, int 
   float* s_x = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(M) * K * 2));
   int st = launch_pack(X, x_dtype, M, K, G, x16, kPackF16, s_x, s, input_scale);
   if (st) return st;
-  return launch_grouped(x16, s_x, M, K, weights, n_weights, s, input_scale);
+  return launch_grouped(x16, s_x, M, K, weights, n_weights, s, input_scale,
+                        sync_at(ws + need - CONVROT_GEMM_SYNC_BYTES));
 }
 
 int convrot_pack_prologue(const float* X, int64_t M, int64_t K, int G, const convrot_prologue* pro,
@@ -402,7 +421,7 @@ int convrot_linear_prologue(const float* X, int64_t M, int64_t K, int G, const c
   int st = launch_pack_modulated(X, M, K, G, pro->weight, pro->scale, pro->shift, pro->rmsnorm != 0, pro->eps, x16,
                                  kPackF16, s_x, s);
   if (st) return st;
-  return launch_grouped(x16, s_x, M, K, weights, n_weights, s);
+  return launch_grouped(x16, s_x, M, K, weights, n_weights, s, 1.0f, sync_at(ws + need - CONVROT_GEMM_SYNC_BYTES));
 }
 
 int convrot_w4_expand(const uint8_t* Q_w4, int64_t N, int64_t K, int8_t* Q_w, uint16_t* Q_w16, void* stream) {

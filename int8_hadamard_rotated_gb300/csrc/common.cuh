@@ -159,6 +159,19 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   return r != 0;
 }
 
+// gpu-scope flag words
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_relaxed_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
 // Untiled bulk copy shared -> global (both 16-byte aligned, bytes % 16 == 0),
 // tracked by the issuing thread's bulk-async groups.
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
@@ -431,9 +444,25 @@ struct GemmLinear {
 // Exact-chunk plan of int8 weight codes (see convrot_weight_chunks).
 int launch_chunk_plan(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, cudaStream_t stream);
 
+// Device words through which the CTA pairs of one GEMM launch hand partial
+// sums of split tiles to each other (the balanced tail): CONVROT_GEMM_SYNC_BYTES
+// of caller scratch, 16-byte aligned, not used by any other launch while the
+// GEMM runs. Words the GEMM consumes are left zero for the next launch. With no
+// words the GEMM takes whole tiles only.
+struct GemmSync {
+  unsigned long long* words = nullptr;
+  size_t bytes = 0;
+};
+
+// The hand-over words at `base` (CONVROT_GEMM_SYNC_BYTES of workspace).
+inline GemmSync sync_at(void* base) {
+  return GemmSync{static_cast<unsigned long long*>(base), CONVROT_GEMM_SYNC_BYTES};
+}
+
 // out_j = epilogue(x16 . w16_j^T) for every linear j; raw_s32 selects int32 A.
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream);
+                const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
+                GemmSync sync = GemmSync());
 
 // ---------------------------------------------------------------------------
 // host-side checks and the grouped launch shared by the entry points (api.cu)
@@ -447,6 +476,7 @@ int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64
                   const void* in0, size_t n0, const void* in1, size_t n1);
 // One grouped GEMM over the non-empty linears, on packed fp16 codes + s_x.
 int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale = 1.0f);
+                   const convrot_weight* weights, int n_weights, cudaStream_t s, float in_scale = 1.0f,
+                   GemmSync sync = GemmSync());
 
 }  // namespace convrot

@@ -42,6 +42,9 @@
 #include "common.cuh"
 
 #include <cuda.h>
+#include <algorithm>
+#include <atomic>
+#include <chrono>
 #include <mutex>
 
 namespace convrot {
@@ -61,7 +64,8 @@ constexpr int MMA_WARP = NUM_EPI_WARPS + 1;
 constexpr int THREADS = (NUM_EPI_WARPS + 2) * 32;
 constexpr int TMEM_COLS = 512;       // two fp32 accumulators of BN columns each
 constexpr int MAX_LIN = CONVROT_MAX_LINEARS;
-constexpr int RASTER_BANDS = 8;       // activation bands per raster group
+constexpr int64_t RASTER_L2_BYTES = 48ll << 20;  // activation codes a raster group keeps in L2
+constexpr int EPI_BAR = 3;            // named barrier of the eight epilogue warps (1, 2: per warpgroup)
 
 static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
@@ -114,27 +118,109 @@ struct GemmParams {
   int n_xtiles;                    // ceil(M / BN) activation bands
   int n_wtiles;                    // sum over linears of ceil(N_j / TILE_M)
   int total_tiles;
+  int raster_bands;                // activation bands per raster group
   int n_lin;
   int raw_s32;
+  // Balanced waves: the K blocks of the first sk_tiles tiles (0 = none) are
+  // split into one contiguous range per unit, done first; the other tiles are
+  // then taken whole, round-robin over the units. A unit whose range ends
+  // inside a tile stores its int32 partial sums in that tile's output and
+  // publishes `epoch` in its flag word; the unit whose range finishes the
+  // tile adds them. Split tiles come first so that this hand-over overlaps
+  // the whole tiles' MMAs instead of lengthening the last wave.
+  int sk_tiles;
+  unsigned long long* sk_flags;    // [2 * units]: one word per CTA of a pair
+  unsigned long long epoch;        // nonzero, distinct per launch
 };
 
 struct TileCoord {
   int lin, wt, xt;
 };
 
-// Raster order: tiles are taken in groups of RASTER_BANDS activation bands;
-// inside a group, consecutive tiles walk the bands of one weight tile before
-// moving to the next weight tile (of the same or the next linear). The tiles
-// in flight then cover ~RASTER_BANDS bands and a few dozen weight tiles,
-// which stay in L2 while the group is swept.
+// One piece of a unit's work: K blocks [kb0, kb1) of tile t.
+enum : int {
+  kWhole = 0,  // the whole tile
+  kHead = 1,   // the tile's first K blocks: partial sums go to the next unit
+  kTail = 2,   // the tile's last K blocks: adds the previous unit's partial sums
+};
+struct WorkItem {
+  int t, kb0, kb1, kind;
+};
+
+// Item j of a unit's work: first its K-block range of the split tiles, from
+// the highest tile down, so that the head it hands on comes first and the
+// tail it finishes last; then its whole tiles. Every range is at least one
+// tile long (sk_tiles >= units), so a split tile has exactly one head and one
+// tail, and the tail's unit is the head's plus one. Items are recomputed from
+// j rather than carried, to keep the epilogue's registers for its
+// accumulators.
+__device__ __forceinline__ bool work_item(const GemmParams& p, int unit, int n_units, int j, WorkItem& it) {
+  int n_sk = 0;
+  if (p.sk_tiles > 0) {
+    const long long total = static_cast<long long>(p.sk_tiles) * p.num_kb;
+    const int s = static_cast<int>(total * unit / n_units);
+    const int e = static_cast<int>(total * (unit + 1) / n_units);
+    const int hi = (e - 1) / p.num_kb;
+    n_sk = hi - s / p.num_kb + 1;
+    if (j < n_sk) {
+      const int tile = hi - j;
+      const int base = tile * p.num_kb;
+      it.t = tile;
+      it.kb0 = max(0, s - base);
+      it.kb1 = min(p.num_kb, e - base);
+      it.kind = (it.kb1 < p.num_kb) ? kHead : (it.kb0 > 0 ? kTail : kWhole);
+      return true;
+    }
+  }
+  const int t = p.sk_tiles + unit + (j - n_sk) * n_units;
+  if (t >= p.total_tiles) return false;
+  it.t = t;
+  it.kb0 = 0;
+  it.kb1 = p.num_kb;
+  it.kind = kWhole;
+  return true;
+}
+
+// End of the exact chunk that starts at K block c0 (chunks are aligned runs of
+// L blocks inside a tile), clipped to kb1.
+__device__ __forceinline__ int chunk_end(int c0, int L, int kb1) {
+  return min(kb1, (c0 / L + 1) * L);
+}
+
+// Bounded wait until *flag == v (acquire). On giving up: sets the CTA's abort
+// flag, records CONVROT_ERR_TIMEOUT and returns false.
+__device__ __forceinline__ bool wait_flag(const unsigned long long* flag, unsigned long long v,
+                                          volatile int* abort_flag, int* err) {
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(flag) == v) return true;
+    if ((it & 15) == 15) {
+      if (*abort_flag) return false;
+      if (global_timer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        record_error(err, CONVROT_ERR_TIMEOUT);
+        return false;
+      }
+    }
+    __nanosleep(128);
+  }
+}
+
+// Raster order: tiles are taken in groups of raster_bands activation bands
+// (as many as fit RASTER_L2_BYTES of codes; all of them for the usual
+// shapes); inside a group, consecutive tiles walk the bands of one weight
+// tile before moving to the next weight tile (of the same or the next
+// linear). The group's activation codes then stay in L2 while its weight
+// tiles stream through once.
 __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
-  const int per_group = RASTER_BANDS * p.n_wtiles;
+  const int rb = p.raster_bands;
+  const int per_group = rb * p.n_wtiles;
   const int g = t / per_group;
   const int idx = t - g * per_group;
-  const int gm = min(RASTER_BANDS, p.n_xtiles - g * RASTER_BANDS);
+  const int gm = min(rb, p.n_xtiles - g * rb);
   const int w = idx / gm;
   TileCoord c;
-  c.xt = g * RASTER_BANDS + (idx - w * gm);
+  c.xt = g * rb + (idx - w * gm);
   int j = 0;
 #pragma unroll 1
   while (j + 1 < p.n_lin && w >= p.wtile_start[j + 1]) ++j;
@@ -234,11 +320,12 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       uint32_t stage = 0, phase = 0;
       uint32_t n_issued = 0;  // stage loads issued so far (stage = n % STAGES)
       bool ok = true;
-      for (int t = unit; ok && t < p.total_tiles; t += n_units) {
-        const TileCoord c = decode_tile(p, t);
+      WorkItem it;
+      for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
+        const TileCoord c = decode_tile(p, it.t);
         const int w_row = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
         const int x_row = c.xt * BN + static_cast<int>(rank) * Gm::X_ROWS;
-        for (int kb = 0; kb < p.num_kb; ++kb) {
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
           uint8_t* sw = smem + stage * Gm::STAGE_BYTES;
           uint8_t* sx = sw + Gm::W_BYTES;
@@ -271,20 +358,24 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, chunk_iter = 0;
       bool ok = true;
-      // the next tile's chunk length is read one tile ahead
-      int L_next = (unit < p.total_tiles) ? tile_chunk_kb<CG>(p, decode_tile(p, unit)) : 1;
-      for (int t = unit; ok && t < p.total_tiles; t += n_units) {
-        const int L = L_next;
-        if (t + n_units < p.total_tiles) L_next = tile_chunk_kb<CG>(p, decode_tile(p, t + n_units));
-        const int num_chunks = (p.num_kb + L - 1) / L;
-        for (int ch = 0; ok && ch < num_chunks; ++ch) {
+      // the next item's chunk length is read one item ahead
+      WorkItem it, nx;
+      int j = 0;
+      bool have = work_item(p, unit, n_units, j, it);
+      int L = have ? tile_chunk_kb<CG>(p, decode_tile(p, it.t)) : 1;
+      while (ok && have) {
+        const bool have_nx = work_item(p, unit, n_units, ++j, nx);
+        const int L_nx = have_nx ? tile_chunk_kb<CG>(p, decode_tile(p, nx.t)) : 1;
+        for (int c0 = it.kb0; ok && c0 < it.kb1;) {
+          const int c1 = chunk_end(c0, L, it.kb1);
           const uint32_t buf = chunk_iter & 1u;
           const uint32_t use = chunk_iter >> 1;
           if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
-          const int kb0 = ch * L;
-          const int kb1 = min(kb0 + L, p.num_kb);
+          const int kb0 = c0;
+          const int kb1 = c1;
+          c0 = c1;
           for (int kb = kb0; kb < kb1; ++kb) {
             if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
             tc_fence_after();
@@ -306,6 +397,9 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           if (CG == 2) mma_commit_pair(&tfull[buf], 0x3); else mma_commit(&tfull[buf]);
           ++chunk_iter;
         }
+        it = nx;
+        L = L_nx;
+        have = have_nx;
       }
       // all issued MMAs complete before TMEM is released
       if (CG == 2) mma_commit_pair(drain, 0x1); else mma_commit(drain);
@@ -322,14 +416,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     const uint32_t tempty_leader = (CG == 2) ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
     uint32_t chunk_iter = 0;
     bool ok = true;
-    for (int t = unit; ok && t < p.total_tiles; t += n_units) {
-      const TileCoord c = decode_tile(p, t);
+    WorkItem it;
+    for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
+      const TileCoord c = decode_tile(p, it.t);
       const int L = tile_chunk_kb<CG>(p, c);
-      const int num_chunks = (p.num_kb + L - 1) / L;
       int acc[COLS_PER_THREAD];
 #pragma unroll
       for (int i = 0; i < COLS_PER_THREAD; ++i) acc[i] = 0;
-      for (int ch = 0; ch < num_chunks; ++ch) {
+      for (int c0 = it.kb0; c0 < it.kb1; c0 = chunk_end(c0, L, it.kb1)) {
         const uint32_t buf = chunk_iter & 1u;
         const uint32_t use = chunk_iter >> 1;
         if (!mbar_wait(&tfull[buf], use & 1u, abort_flag, err)) { ok = false; break; }
@@ -350,13 +444,54 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         }
         ++chunk_iter;
       }
-      // the warpgroup leaves together (its stores use a barrier of its own)
-      if (YTMA) ok = named_bar_and(1 + half, 4 * 32, ok);
+      // the eight epilogue warps leave together (the Y stores and the hand-over
+      // of split tiles use barriers of their own)
+      ok = named_bar_and(EPI_BAR, NUM_EPI_WARPS * 32, ok);
       if (!ok) break;
       const int N = p.N[c.lin];
       const int o = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
       const bool o_ok = o < N;
       const int r0 = c.xt * BN + half * COLS_PER_THREAD;
+      // partial sums of a split tile travel through the tile's own output, as int32
+      int32_t* part = static_cast<int32_t*>(p.out[c.lin]);
+      if (it.kind == kHead) {
+        if (o_ok) {
+#pragma unroll
+          for (int i = 0; i < COLS_PER_THREAD; ++i) {
+            const int r = r0 + i;
+            if (r < p.M) part[static_cast<int64_t>(r) * N + o] = acc[i];
+          }
+        }
+        __threadfence();
+        named_bar_sync(EPI_BAR, NUM_EPI_WARPS * 32);
+        if (threadIdx.x == 0) st_release_gpu(p.sk_flags + 2 * unit + rank, p.epoch);
+        continue;
+      }
+      if (it.kind == kTail) {
+        bool got = true;
+        if (threadIdx.x == 0) {
+          unsigned long long* f = p.sk_flags + 2 * (unit - 1) + rank;
+          got = wait_flag(f, p.epoch, abort_flag, err);
+          if (got) st_relaxed_gpu(f, 0ull);  // consumed: zero again for the next launch
+        }
+        ok = named_bar_and(EPI_BAR, NUM_EPI_WARPS * 32, got);
+        if (!ok) break;
+        if (o_ok) {
+          // 16 loads in flight at a time (L2 only: the partial sums were
+          // written by another SM)
+#pragma unroll
+          for (int q = 0; q < COLS_PER_THREAD / 16; ++q) {
+            int32_t v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int r = r0 + 16 * q + i;
+              v[i] = (r < p.M) ? __ldcg(part + static_cast<int64_t>(r) * N + o) : 0;
+            }
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[16 * q + i] += v[i];
+          }
+        }
+      }
       if (p.raw_s32) {
         if (o_ok) {
           int32_t* A = static_cast<int32_t*>(p.out[c.lin]);
@@ -500,12 +635,52 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
   p.num_kb = static_cast<int>((K + BK - 1) / BK);
   p.n_xtiles = static_cast<int>((M + BN - 1) / BN);
   p.n_wtiles = wt;
+  const int64_t band_bytes = static_cast<int64_t>(BN) * K * 2;
+  p.raster_bands = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.n_xtiles, RASTER_L2_BYTES / band_bytes)));
   const int64_t total = static_cast<int64_t>(p.n_xtiles) * wt;
   if (total > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
   p.total_tiles = static_cast<int>(total);
   p.n_lin = n_lin;
   p.raw_s32 = raw_s32 ? 1 : 0;
+  p.sk_tiles = 0;
   return CONVROT_OK;
+}
+
+// Nonzero value distinct per launch for the hand-over flags: a process-wide
+// counter that starts at the wall clock in nanoseconds, so that flag words
+// left in reused scratch by an earlier launch or process never match.
+unsigned long long next_epoch() {
+  static std::atomic<unsigned long long> counter{
+      static_cast<unsigned long long>(std::chrono::duration_cast<std::chrono::nanoseconds>(
+                                          std::chrono::system_clock::now().time_since_epoch())
+                                          .count()) |
+      1ull};
+  return counter.fetch_add(1);
+}
+
+// Whole tiles only, or split tiles first, for `units` co-resident units. The
+// split takes the fractional wave and one whole wave (so that every unit's
+// range covers at least one tile) and is used only where it pays on this
+// GPU: when a last wave of whole tiles would leave at least 40 % of the units
+// idle and at least one whole wave remains after the split. (A last wave
+// that is busier runs nearly as fast as the split: with fewer tiles in
+// flight each runs faster. Splitting every tile adds the partial-sum
+// hand-over to the end of the kernel.)
+bool split_pays(int T, int units) {
+  if (units < 2 || T < 2 * units) return false;
+  const int rem = T % units;
+  return rem != 0 && 10 * (units - rem) >= 4 * units;
+}
+
+void plan_split(GemmParams& p, int units, const GemmSync& sync) {
+  p.sk_tiles = 0;
+  const int T = p.total_tiles;
+  if (!sync.words || sync.bytes < static_cast<size_t>(2 * units) * sizeof(unsigned long long)) return;
+  if (!split_pays(T, units)) return;
+  const int rem = T % units;
+  p.sk_tiles = units + rem;
+  p.sk_flags = sync.words;
+  p.epoch = next_epoch();
 }
 
 // Raise the kernel's shared-memory limit once per device.
@@ -573,16 +748,17 @@ int max_pairs() {
 
 template <int BN, bool UNSCALE, bool YTMA>
 int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
-                 bool raw_s32, int pairs, cudaStream_t stream) {
+                 bool raw_s32, int pairs, cudaStream_t stream, const GemmSync& sync) {
   GemmParams p;
   if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
   if (YTMA)
     for (int j = 0; j < n_lin; ++j)
       if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
+  const int units = std::min(p.total_tiles, pairs);
+  if (BN == 256) plan_split(p, units, sync);
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg =
-      pair_config(std::min(p.total_tiles, pairs), Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true);
+  const cudaLaunchConfig_t cfg = pair_config(units, Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true);
   if (int st = configure_kernel<2, BN, UNSCALE, YTMA>()) return st;
   cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE, YTMA>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
@@ -666,25 +842,30 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// Activation rows per tile: the tile height among 256, 192 and 128 whose
-// last wave of pair tiles is least empty. Modelled time: waves x (BN + 32),
-// the 32 standing for the fixed cost of a tile; ties go to the taller tile.
-int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs) {
+// Activation rows per tile: the tile height among 256, 192 and 128 with the
+// least modelled time, waves x (BN + 96), where waves counts a partial last
+// wave as a whole one unless the split will balance it (256-row tiles; then
+// the fraction counts), and 96 stands for the cost of a tile that does not
+// shrink with its height (the weight rows it streams); ties go to the taller
+// tile.
+int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool can_split) {
   int64_t wtiles = 0;
   for (int j = 0; j < n_lin; ++j) wtiles += (lins[j].N + 2 * CTA_M - 1) / (2 * CTA_M);
   int best = 256;
-  int64_t best_cost = -1;
+  double best_cost = -1.0;
   for (int bn : {256, 192, 128}) {
     const int64_t tiles = ((M + bn - 1) / bn) * wtiles;
-    const int64_t waves = (tiles + pairs - 1) / pairs;
-    const int64_t cost = waves * (bn + 32);
-    if (best_cost < 0 || cost < best_cost) { best = bn; best_cost = cost; }
+    // only 256-row tiles are split (shorter tiles lose more than the split gains)
+    const bool split = can_split && bn == 256 && tiles <= 0x7fffffff && split_pays(static_cast<int>(tiles), pairs);
+    const double waves = split ? static_cast<double>(tiles) / pairs : static_cast<double>((tiles + pairs - 1) / pairs);
+    const double cost = waves * (bn + 96);
+    if (best_cost < 0.0 || cost < best_cost) { best = bn; best_cost = cost; }
   }
   return best;
 }
 
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
-                const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream) {
+                const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream, GemmSync sync) {
   if (M == 0) return CONVROT_OK;
   bool unscale = false, ytma = !raw_s32;
   for (int j = 0; j < n_lin; ++j) {
@@ -697,20 +878,21 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
   if (int st = configure_kernel<2, 128, false, true>()) return st;
   const int pairs = std::min(max_pairs<256>(), std::min(max_pairs<192>(), max_pairs<128>()));
   if (pairs > 0) {
-    const int bn = pick_tile_rows(M, lins, n_lin, pairs);
+    const bool can_split = sync.words && sync.bytes >= static_cast<size_t>(2 * pairs) * sizeof(unsigned long long);
+    const int bn = pick_tile_rows(M, lins, n_lin, pairs, can_split);
     if (ytma) {
-      if (bn == 128) return launch_pairs<128, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      if (bn == 192) return launch_pairs<192, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      return launch_pairs<256, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      if (bn == 128) return launch_pairs<128, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      if (bn == 192) return launch_pairs<192, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      return launch_pairs<256, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
     }
     if (unscale) {
-      if (bn == 128) return launch_pairs<128, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      if (bn == 192) return launch_pairs<192, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-      return launch_pairs<256, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+      if (bn == 128) return launch_pairs<128, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      if (bn == 192) return launch_pairs<192, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      return launch_pairs<256, true, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
     }
-    if (bn == 128) return launch_pairs<128, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-    if (bn == 192) return launch_pairs<192, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
-    return launch_pairs<256, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream);
+    if (bn == 128) return launch_pairs<128, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+    if (bn == 192) return launch_pairs<192, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+    return launch_pairs<256, false, false>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
   }
   GemmParams p;
   if (int st = fill_params<1, 256>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;

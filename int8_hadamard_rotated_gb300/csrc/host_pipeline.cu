@@ -84,7 +84,7 @@ extern "C" size_t convrot_linear_host_workspace_size(int64_t M, int64_t K, int x
                                                      int64_t chunk_rows) {
   if (M <= 0 || K <= 0 || n_total < 0 || chunk_rows < 0) return 0;
   if (x_dtype != CONVROT_F32 && x_dtype != CONVROT_F16) return 0;
-  return 2 * buffer_set_bytes(chunk_rows_for(M, chunk_rows), K, x_dtype, n_total);
+  return 2 * buffer_set_bytes(chunk_rows_for(M, chunk_rows), K, x_dtype, n_total) + CONVROT_GEMM_SYNC_BYTES;
 }
 
 extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, int64_t K, int G,
@@ -129,6 +129,7 @@ extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, i
   const size_t set_bytes = buffer_set_bytes(cr, K, x_dtype, n_total);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   const ChunkBuffers B[2] = {carve(ws, cr, K, x_dtype), carve(ws + set_bytes, cr, K, x_dtype)};
+  const GemmSync sync = sync_at(ws + 2 * set_bytes);  // the chunks' GEMMs run one after the other on `stream`
   const size_t esz = esize(x_dtype);
   const uint8_t* xh = static_cast<const uint8_t*>(X_host);
   const int64_t nchunks = (M + cr - 1) / cr;
@@ -156,7 +157,7 @@ extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, i
       off += static_cast<size_t>(m) * w.N;
     }
     if (n > 0)
-      if (int st = launch_gemm(B[b].q16, B[b].s_x, m, K, lins, n, false, s)) return st;
+      if (int st = launch_gemm(B[b].q16, B[b].s_x, m, K, lins, n, false, s, sync)) return st;
     CONVROT_TRY(cudaEventRecord(ev.done[b], s));
     // copy out every linear's rows of this chunk (contiguous in both places)
     CONVROT_TRY(cudaStreamWaitEvent(sout, ev.done[b], 0));

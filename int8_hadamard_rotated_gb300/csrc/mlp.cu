@@ -13,7 +13,7 @@ namespace convrot {
 namespace {
 
 struct MlpLayout {
-  size_t x16, s_x, h, h16, s_h, total;
+  size_t x16, s_x, h, h16, s_h, sync, total;
 };
 
 MlpLayout mlp_layout(int64_t M, int64_t K, int64_t N_up) {
@@ -24,7 +24,8 @@ MlpLayout mlp_layout(int64_t M, int64_t K, int64_t N_up) {
   l.h = l.s_x + round256(m * 4);
   l.h16 = l.h + round256(m * N_up * 4);
   l.s_h = l.h16 + round256(m * N_up * 2);
-  l.total = l.s_h + round256(m * 4);
+  l.sync = l.s_h + round256(m * 4);
+  l.total = l.sync + CONVROT_GEMM_SYNC_BYTES;
   return l;
 }
 
@@ -77,11 +78,12 @@ extern "C" int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int
   float* s_h = reinterpret_cast<float*>(ws + l.s_h);
   if (int st = launch_pack(X, x_dtype, M, K, G_up, x16, kPackF16, s_x, s)) return st;
   GemmLinear lu{reinterpret_cast<const __half*>(up->q16), up->scale, up->bias, H, N_up, up->kchunk};
-  if (int st = launch_gemm(x16, s_x, M, K, &lu, 1, false, s)) return st;
+  const GemmSync sync = sync_at(ws + l.sync);  // the two GEMMs run one after the other
+  if (int st = launch_gemm(x16, s_x, M, K, &lu, 1, false, s, sync)) return st;
   int st = (activation == CONVROT_ACT_GELU) ? launch_pack_gelu(H, M, N_up, G_down, h16, s_h, s)
                                              : launch_pack(H, CONVROT_F32, M, N_up, G_down, h16, kPackF16, s_h, s);
   if (st) return st;
   GemmLinear ld{reinterpret_cast<const __half*>(down->q16), down->scale, down->bias, down->Y, down->N,
                 down->kchunk};
-  return launch_gemm(h16, s_h, M, N_up, &ld, 1, false, s);
+  return launch_gemm(h16, s_h, M, N_up, &ld, 1, false, s, sync);
 }

@@ -42,6 +42,7 @@ PACK_MAX_K = 32768
 MAX_K = 133144
 CHUNK_ROWS = 128
 NOALLOC_SCRATCH_BYTES = 32 << 20
+GEMM_SYNC_BYTES = 4096
 
 
 class ConvrotError(RuntimeError):
@@ -87,7 +88,7 @@ SIGNATURES = {
     "convrot_weight_chunks": (_I, [_VP, _I64, _I64, _VP, _VP]),
     "convrot_w4_expand": (_I, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
-    "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP]),
+    "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
     "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
     "convrot_linear_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I64, _VP, _SZ,
                                  _VP, _VP, _VP]),
@@ -365,8 +366,12 @@ def convrot_pack_activations_f16(X: torch.Tensor, G: int, Q_x16: Optional[torch.
 
 
 def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases,
-                          Ys=None, stream=None, weights=None, kchunks=None):
-    """Grouped GEMM on an already packed activation (fp16 codes + row scales)."""
+                          Ys=None, stream=None, weights=None, kchunks=None, workspace=None,
+                          split_tail: bool = True):
+    """Grouped GEMM on an already packed activation (fp16 codes + row scales).
+    With split_tail (the default) the GEMM gets GEMM_SYNC_BYTES of scratch
+    (`workspace`, or a fresh buffer) and may split its last wave of tiles by K;
+    split_tail=False passes none (whole tiles only; same results)."""
     _need(Q_x16, torch.float16, "Q_x16")
     _need(s_x, torch.float32, "s_x")
     M, K = Q_x16.shape
@@ -374,7 +379,12 @@ def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, 
         Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=Q_x16.device) for q in q16s]
     if weights is None:
         weights = make_weights(q16s, scales, biases, Ys, kchunks)
-    _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _stream(stream)),
+    ws_ptr, ws_bytes = None, 0
+    if split_tail:
+        ws = _workspace(GEMM_SYNC_BYTES, Q_x16.device, workspace)
+        ws_ptr, ws_bytes = _ptr(ws), ws.numel() * ws.element_size()
+    _check(lib().convrot_linear_packed(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), ws_ptr, ws_bytes,
+                                       _stream(stream)),
            "convrot_linear_packed")
     return Ys
 

@@ -50,13 +50,34 @@ def test_strerror_and_version(L):
 
 
 def test_workspace_sizes(L):
-    assert L.convrot_linear_workspace_size(4608, 3072) == 4608 * 3072 * 2 + ((4608 * 4 + 255) // 256) * 256
-    assert L.int8_linear_workspace_size(16, 128, 256, 1) == 16 * 256 * 2
-    assert L.int8_linear_workspace_size(16, 128, 256, 0) == 16 * 256 * 2 + 128 * 256 * 2
+    from int8_hadamard_rotated_gb300 import ops
+    sync = ops.GEMM_SYNC_BYTES  # the GEMM's hand-over words, one 8-byte word per CTA of up to 256 pairs
+    assert sync == 2 * 256 * 8
+    assert L.convrot_linear_workspace_size(4608, 3072) == 4608 * 3072 * 2 + ((4608 * 4 + 255) // 256) * 256 + sync
+    assert L.int8_linear_workspace_size(16, 128, 256, 1) == 16 * 256 * 2 + sync
+    assert L.int8_linear_workspace_size(16, 128, 256, 0) == 16 * 256 * 2 + 128 * 256 * 2 + sync
+    m = 4608 * 3072 * 2 + 4608 * 4 + 4608 * 12288 * 4 + 4608 * 12288 * 2 + 4608 * 4
+    assert L.convrot_mlp_workspace_size(4608, 3072, 12288) == m + sync
+
+
+def test_packed_linear_workspace_checks(L):
+    """convrot_linear_packed: the hand-over workspace is optional, but when
+    given it must be aligned, large enough and apart from every other array
+    (checked before any device call)."""
+    from int8_hadamard_rotated_gb300 import ops
+    W = ops.convrot_weight
+    wts = (W * 1)(W(A1, A2, A3, 64, A4, None))
+    f = L.convrot_linear_packed
+    sync = ops.GEMM_SYNC_BYTES
+    assert f(A0, A5, 16, 256, wts, 1, A6 + 8, sync, None) == ops.ERR_ALIGN
+    assert f(A0, A5, 16, 256, wts, 1, A6, sync - 1, None) == ops.ERR_WORKSPACE
+    assert f(A0, A5, 16, 256, wts, 1, A4, sync, None) == ops.ERR_ALIAS       # on Y
+    assert f(A0, A5, 16, 256, wts, 1, A0 + 256, sync, None) == ops.ERR_ALIAS  # inside Q_x16
+    assert f(A0, A5, 0, 256, wts, 1, None, 0, None) == ops.OK
 
 
 # fake, 256-aligned, non-overlapping device addresses
-A0, A1, A2, A3, A4, A5 = (0x7f0000000000 + i * 0x10000000 for i in range(6))
+A0, A1, A2, A3, A4, A5, A6 = (0x7f0000000000 + i * 0x10000000 for i in range(7))
 
 
 def test_pack_argument_checks(L):
@@ -128,7 +149,7 @@ def test_host_pipeline_checks(L):
     # two sets of (input rows, binary16 codes, scales, outputs), each rounded to 256 bytes
     r = 768
     one = (r * 3072 * 4) + (r * 3072 * 2) + ((r * 4 + 255) // 256 * 256) + (r * 9216 * 4)
-    assert ws(4608, 3072, ops.F32, 9216, 0) == 2 * one
+    assert ws(4608, 3072, ops.F32, 9216, 0) == 2 * one + ops.GEMM_SYNC_BYTES
     assert ws(100, 3072, ops.F32, 9216, 0) == ws(100, 3072, ops.F32, 9216, 100)  # chunk clipped to M
     assert ws(0, 3072, ops.F32, 9216, 0) == 0 and ws(10, 3072, 5, 9216, 0) == 0
     W = ops.convrot_weight
