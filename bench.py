@@ -422,6 +422,8 @@ def run_gpu(args, rank, world, local_rank):
            "ops_per_call": int(mw.gemm_ops)}
     del Xm, mlp_w, Ym, wsm
 
+    library = library_gemm_same_shape(w, dev, flush, float(gemm_ms.mean() * 1e3)) if args.library_gemm else None
+
     pack = {
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
         "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
@@ -445,7 +447,40 @@ def run_gpu(args, rank, world, local_rank):
                    "gemm_us_mean_alone": float(gemm_ms.mean() * 1e3), "wall_s_timed_loop": wall},
         "e2e_parity_max_abs_diff": float(max((a - b).abs().max().item() for a, b in zip(Yt, Y_host))),
     }
+    if library is not None:
+        result["library_gemm_same_shape"] = library
     return result, case, w
+
+
+def library_gemm_same_shape(w, dev, flush, ours_us, reps=20):
+    """Context for the GEMM roofline: cuBLAS (through torch.mm) on the same
+    shape, M x sum(N) x K with binary16 operands and fp32 output, L2 flushed
+    before each call like the timed steps. Not part of the step."""
+    n = sum(w.Ns)
+    a = torch.randn(w.M, w.K, device=dev).half()
+    b = torch.randn(n, w.K, device=dev).half()
+    try:
+        fn = lambda: torch.mm(a, b.t(), out_dtype=torch.float32)
+        fn()
+    except (TypeError, RuntimeError) as e:
+        return {"unavailable": f"torch.mm with out_dtype: {type(e).__name__}"}
+    for _ in range(3):
+        flush.zero_()
+        fn()
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        fn()
+        e1.record()
+        ev.append((e0, e1))
+    torch.cuda.synchronize()
+    us = float(np.mean([x.elapsed_time(y) for x, y in ev])) * 1e3
+    ops = 2.0 * w.M * n * w.K
+    return {"kernel": "cuBLAS binary16 x binary16 -> fp32 (torch.mm, out_dtype=float32), no reconstruction",
+            "shape": [w.M, n, w.K], "us": round(us, 2), "TFLOP/s": round(ops / (us * 1e-6) / 1e12, 1),
+            "ours_gemm_us": round(ours_us, 2)}
 
 
 def run_reference(args, rank):
@@ -486,6 +521,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-library-gemm", dest="library_gemm", action="store_false",
+                    help="skip timing cuBLAS on the GEMM's shape (context for the roofline)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
