@@ -456,6 +456,7 @@ def library_gemm_same_shape(w, dev, flush, ours_us, reps=20):
     """Context for the GEMM roofline: cuBLAS (through torch.mm) on the same
     shape, M x sum(N) x K with binary16 operands and fp32 output, L2 flushed
     before each call like the timed steps. Not part of the step."""
+    import torch
     n = sum(w.Ns)
     a = torch.randn(w.M, w.K, device=dev).half()
     b = torch.randn(n, w.K, device=dev).half()
