@@ -366,6 +366,34 @@ def run_gpu(args, rank, world, local_rank):
         ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
         gbs = pack_bytes / (ms * 1e-3) / 1e9
         sweep[str(G)] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+    # the same packs back to back over rotating buffers (together more than
+    # 4x L2, so no launch finds its input in L2): kernel throughput without
+    # the launch latency that an isolated launch after a flush includes
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    nbuf = max(2, -(-4 * l2 // (pw.M * pw.K * 4)))
+    Xr = [Xp.clone() for _ in range(nbuf)]
+    Qr = [torch.empty_like(Qp) for _ in range(nbuf)]
+    sr = [torch.empty_like(sp_x) for _ in range(nbuf)]
+    passes = 3
+    for G in pw.groups:
+        def run_all():
+            for i in range(nbuf):
+                st = L.convrot_pack_activations(Xr[i].data_ptr(), ops.F32, pw.M, pw.K, G, Qr[i].data_ptr(),
+                                                sr[i].data_ptr(), sp)
+                if st:
+                    raise ops.ConvrotError(st, "pack sweep")
+        run_all()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(passes):
+            run_all()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / (passes * nbuf)
+        gbs = pack_bytes / (ms * 1e-3) / 1e9
+        sweep[str(G)]["back_to_back"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+                                         "buffers": nbuf}
+    del Xr, Qr, sr
     # long rows: the MLP pair's repack input, X fp32 [4608, 12288] -> binary16 codes
     ML, KL = 4608, 12288
     gen = torch.Generator(device=dev)
@@ -428,6 +456,8 @@ def run_gpu(args, rank, world, local_rank):
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
         "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
         "peak_kind": f"{peak_kind} HBM copy", "by_group": sweep,
+        "by_group_note": "us/GB/s/frac: isolated launches, L2 flushed before each (launch latency included); "
+                         "back_to_back: consecutive launches over rotating buffers larger than 4x L2",
         "fused_step_pack": {"us": round(float(pack_ms.mean()) * 1e3, 2),
                             "bytes": fused_pack_bytes,
                             "GB/s": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9, 1),
