@@ -183,6 +183,26 @@ __device__ __forceinline__ bool work_item(const GemmParams& p, int unit, int n_u
   return true;
 }
 
+// Lane-wise IEEE fp32 pairs (each lane rounded as the scalar operation).
+__device__ __forceinline__ unsigned long long pair_f32(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpair_f32(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long mul_f32x2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
 // End of the exact chunk that starts at K block c0 (chunks are aligned runs of
 // L blocks inside a tile), clipped to kb1.
 __device__ __forceinline__ int chunk_end(int c0, int L, int kb1) {
@@ -446,6 +466,12 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
       const TileCoord c = decode_tile(p, it.t, static_cast<int>(pair));
       const int L = tile_chunk_kb<CG>(p, c);
+      // One exact chunk (the whole K of a tile that is not split) is kept as
+      // the fp32 value TMEM holds: an integer below 2^24, so it is float(A)
+      // itself. Several chunks, a split tile and the raw int32 output add the
+      // chunks in int32 first.
+      const int n_chunks = (it.kb1 - 1) / L - it.kb0 / L + 1;
+      const bool int_path = p.raw_s32 || n_chunks > 1 || it.kind != kWhole;
       int acc[COLS_PER_THREAD];
 #pragma unroll
       for (int i = 0; i < COLS_PER_THREAD; ++i) acc[i] = 0;
@@ -454,13 +480,24 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const uint32_t use = chunk_iter >> 1;
         if (!mbar_wait(&tfull[buf], use & 1u, abort_flag, err)) { ok = false; break; }
         tc_fence_after();
+        if (int_path) {
 #pragma unroll
-        for (int q = 0; q < COLS_PER_THREAD / 32; ++q) {
-          uint32_t r[32];
-          tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + half * COLS_PER_THREAD + q * 32, r);
-          tmem_ld_wait();
+          for (int q = 0; q < COLS_PER_THREAD / 32; ++q) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + half * COLS_PER_THREAD + q * 32, r);
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) acc[q * 32 + i] += __float2int_rz(__uint_as_float(r[i]));
+            for (int i = 0; i < 32; ++i) acc[q * 32 + i] += __float2int_rz(__uint_as_float(r[i]));
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < COLS_PER_THREAD / 32; ++q) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tmem_base + lane_base + buf * BN + half * COLS_PER_THREAD + q * 32, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) acc[q * 32 + i] = static_cast<int>(r[i]);
+          }
         }
         tc_fence_before();
         __syncwarp();
@@ -528,6 +565,11 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           }
         }
       } else {
+        // from here acc holds float(A) as fp32 bits (the int32 sum rounded to nearest)
+        if (int_path) {
+#pragma unroll
+          for (int i = 0; i < COLS_PER_THREAD; ++i) acc[i] = __float_as_int(__int2float_rn(acc[i]));
+        }
         // the warp's 128 row scales: four per lane, broadcast by shuffles
         float sxv[COLS_PER_THREAD / 32];
 #pragma unroll
@@ -549,19 +591,26 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           const bool store_leader = (quarter == 0 && lane == 0);
           const int col = 32 * quarter + lane;
           const int o_base = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
+          const unsigned long long sw2 = pair_f32(sw, sw), bb2 = pair_f32(bb, bb);
 #pragma unroll
           for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
             if (store_leader) bulk_wait_read<0>();  // the previous store has read the buffer
             named_bar_sync(1 + half, 4 * 32);
 #pragma unroll
-            for (int i = 0; i < Y_ROWS; ++i) {
+            for (int i = 0; i < Y_ROWS; i += 2) {
               const int idx = sub * Y_ROWS + i;
-              const float sx = __shfl_sync(0xffffffffu, sxv[idx >> 5], idx & 31);
-              // float(A) * s_x * s_w + b, one rounding per operation, in that order
-              float y = __fmul_rn(__int2float_rn(acc[idx]), sx);
-              if (sw_ptr) y = __fmul_rn(y, sw);
-              if (b_ptr) y = __fadd_rn(y, bb);
-              sy[i * CTA_M + col] = y;
+              const float sx0 = __shfl_sync(0xffffffffu, sxv[idx >> 5], idx & 31);
+              const float sx1 = __shfl_sync(0xffffffffu, sxv[(idx + 1) >> 5], (idx + 1) & 31);
+              // float(A) * s_x * s_w + b, one rounding per operation, in that
+              // order, for rows idx and idx + 1 at once
+              unsigned long long y = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
+                                               pair_f32(sx0, sx1));
+              if (sw_ptr) y = mul_f32x2(y, sw2);
+              if (b_ptr) y = add_f32x2(y, bb2);
+              float y0, y1;
+              unpair_f32(y, y0, y1);
+              sy[i * CTA_M + col] = y0;
+              sy[(i + 1) * CTA_M + col] = y1;
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + half, 4 * 32);
@@ -577,7 +626,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             const int r = r0 + i;
             if (o_ok && r < p.M) {
               // float(A) * s_x * s_w + b, one rounding per operation, in that order
-              float y = __fmul_rn(__int2float_rn(acc[i]), sx);
+              float y = __fmul_rn(__int_as_float(acc[i]), sx);
               if (sw_ptr) y = __fmul_rn(y, sw);
               if (UNSCALE) y = __fdiv_rn(y, in_scale);  // unscale before the bias
               if (b_ptr) y = __fadd_rn(y, bb);
