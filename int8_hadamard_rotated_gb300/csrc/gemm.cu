@@ -88,7 +88,8 @@ struct Geom {
   static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN);
   // shared-memory layout (after aligning the base to 1024 B)
   static constexpr int SMEM_YOUT = STAGES * STAGE_BYTES;                  // [2][Y_ROWS][128] fp32 (YTMA)
-  static constexpr int SMEM_BARS = SMEM_YOUT + (YTMA ? 2 * Y_HALF_BYTES : 0);  // full[S], empty[S], tfull[2], tempty[2], drain
+  static constexpr int SMEM_SX = SMEM_YOUT + (YTMA ? 2 * Y_HALF_BYTES : 0);  // [2][128] fp32 row scales (YTMA)
+  static constexpr int SMEM_BARS = SMEM_SX + (YTMA ? 2 * 128 * 4 : 0);  // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
   static constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;  // tmem base (u32), abort flag (int)
   // slack for the 1024-B alignment, and (pairs) one more half tile so that
@@ -571,11 +572,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           for (int i = 0; i < COLS_PER_THREAD; ++i) acc[i] = __float_as_int(__int2float_rn(acc[i]));
         }
         // the warp's 128 row scales: four per lane, broadcast by shuffles
+        // (YTMA: the warpgroup's row scales staged in shared memory instead)
         float sxv[COLS_PER_THREAD / 32];
+        if (!YTMA) {
 #pragma unroll
-        for (int k = 0; k < COLS_PER_THREAD / 32; ++k) {
-          const int r = r0 + 32 * k + lane;
-          sxv[k] = (r < p.M) ? __ldg(p.s_x + r) : 0.0f;
+          for (int k = 0; k < COLS_PER_THREAD / 32; ++k) {
+            const int r = r0 + 32 * k + lane;
+            sxv[k] = (r < p.M) ? __ldg(p.s_x + r) : 0.0f;
+          }
         }
         float* Y = static_cast<float*>(p.out[c.lin]);
         const float* sw_ptr = p.s_w[c.lin];
@@ -592,25 +596,41 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           const int col = 32 * quarter + lane;
           const int o_base = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
           const unsigned long long sw2 = pair_f32(sw, sw), bb2 = pair_f32(bb, bb);
+          // the warpgroup's row scales, read back four at a time (a broadcast:
+          // every lane reads the same address); the first barrier below orders
+          // the writes before the reads, and the previous tile's reads ended
+          // before the epilogue-wide barrier of this tile
+          float* ssx = reinterpret_cast<float*>(smem + Gm::SMEM_SX) + half * 128;
+          if (col < COLS_PER_THREAD) ssx[col] = (r0 + col < p.M) ? __ldg(p.s_x + r0 + col) : 0.0f;
 #pragma unroll
           for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
             if (store_leader) bulk_wait_read<0>();  // the previous store has read the buffer
             named_bar_sync(1 + half, 4 * 32);
 #pragma unroll
-            for (int i = 0; i < Y_ROWS; i += 2) {
+            for (int i = 0; i < Y_ROWS; i += 4) {
               const int idx = sub * Y_ROWS + i;
-              const float sx0 = __shfl_sync(0xffffffffu, sxv[idx >> 5], idx & 31);
-              const float sx1 = __shfl_sync(0xffffffffu, sxv[(idx + 1) >> 5], (idx + 1) & 31);
+              const float4 s4 = *reinterpret_cast<const float4*>(ssx + idx);
               // float(A) * s_x * s_w + b, one rounding per operation, in that
-              // order, for rows idx and idx + 1 at once
-              unsigned long long y = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
-                                               pair_f32(sx0, sx1));
-              if (sw_ptr) y = mul_f32x2(y, sw2);
-              if (b_ptr) y = add_f32x2(y, bb2);
-              float y0, y1;
-              unpair_f32(y, y0, y1);
+              // order, two rows at once
+              unsigned long long ya = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
+                                                pair_f32(s4.x, s4.y));
+              unsigned long long yb = mul_f32x2(pair_f32(__int_as_float(acc[idx + 2]), __int_as_float(acc[idx + 3])),
+                                                pair_f32(s4.z, s4.w));
+              if (sw_ptr) {
+                ya = mul_f32x2(ya, sw2);
+                yb = mul_f32x2(yb, sw2);
+              }
+              if (b_ptr) {
+                ya = add_f32x2(ya, bb2);
+                yb = add_f32x2(yb, bb2);
+              }
+              float y0, y1, y2, y3;
+              unpair_f32(ya, y0, y1);
+              unpair_f32(yb, y2, y3);
               sy[i * CTA_M + col] = y0;
               sy[(i + 1) * CTA_M + col] = y1;
+              sy[(i + 2) * CTA_M + col] = y2;
+              sy[(i + 3) * CTA_M + col] = y3;
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + half, 4 * 32);
