@@ -184,6 +184,24 @@ def source_hash():
         return hashlib.sha256(f.read()).hexdigest()
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value over the ranks (the slowest rank's time); x itself
+    with one rank. Every rank must call it (a collective)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tops(ops_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Whole-job throughput in TOPS: the units every rank processed in a step
+    (the same on each: weak scaling) over the slowest rank's step time."""
+    return world * ops_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def run_gpu(args, rank, world, local_rank):
     import torch
     from int8_hadamard_rotated_gb300 import build, ops
@@ -276,13 +294,9 @@ def run_gpu(args, rank, world, local_rank):
     step()
     gemm_ms = time_alone(gemm, reps_alone)
     pack_ms = time_alone(step, reps_alone)
-    ms_step = float(step_ms.mean())
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(float(step_ms.mean()), world, dev)
     ops_step = float(w.gemm_ops)
-    value = world * ops_step / (ms_step * 1e-3) / 1e12
+    value = job_tops(ops_step, ms_step, world)
 
     gemm_tflops = ops_step / (gemm_ms.mean() * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
@@ -324,12 +338,8 @@ def run_gpu(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": world * ops_step / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e = {"value": job_tops(ops_step, e2e_ms, world), "unit": UNIT,
            "h2d_bytes_per_step": int(X_host.numel() * 4),
            "d2h_bytes_per_step": int(sum(y.numel() * 4 for y in Y_host)),
            "ms_per_step": e2e_ms,
