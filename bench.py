@@ -461,6 +461,7 @@ def run_gpu(args, rank, world, local_rank):
     del Xm, mlp_w, Ym, wsm
 
     library = library_gemm_same_shape(w, dev, flush, float(gemm_ms.mean() * 1e3)) if args.library_gemm else None
+    small = small_configs_in_graph(dev) if args.small_configs else None
 
     pack = {
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
@@ -489,7 +490,63 @@ def run_gpu(args, rank, world, local_rank):
     }
     if library is not None:
         result["library_gemm_same_shape"] = library
+    if small is not None:
+        result["small_configs_in_graph"] = small
     return result, case, w
+
+
+def small_configs_in_graph(dev, replays=5):
+    """The small workloads (tiny and UNet-like), one convrot_linear call each
+    (pack + GEMM), timed inside a captured CUDA graph so that launch overhead
+    is amortized: the graph holds one call per set of input, output and
+    workspace buffers, with enough sets (more than 4x L2 in total) that no
+    call finds its data in L2 from the call before. Context, not the step."""
+    import torch
+    from int8_hadamard_rotated_gb300 import ops
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or (126 << 20))
+    out = {}
+    for name in ("tiny", "unet"):
+        w = workloads.get(name)
+        case = workloads.make_case(w)
+        preps = [ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), w.G) for W in case.Ws]
+        q16s, scales = [p[2] for p in preps], [p[1] for p in preps]
+        biases = [torch.from_numpy(b).to(dev) for b in case.bs]
+        plans = [ops.convrot_weight_chunks(p[0]) for p in preps]
+        X0 = torch.from_numpy(case.X).to(dev)
+        per_set = X0.numel() * X0.element_size() + sum(w.M * n * 4 for n in w.Ns)
+        nsets = int(min(256, max(2, -(-4 * l2 // per_set))))
+        Xs = [X0.clone() for _ in range(nsets)]
+        Ys = [[torch.empty((w.M, n), dtype=torch.float32, device=dev) for n in w.Ns] for _ in range(nsets)]
+        wss = [torch.empty((ops.convrot_linear_workspace_size(w.M, w.K),), dtype=torch.uint8, device=dev)
+               for _ in range(nsets)]
+        descs = [ops.make_weights(q16s, scales, biases, Ys[i], plans) for i in range(nsets)]
+
+        def calls():
+            for i in range(nsets):
+                ops.convrot_linear(Xs[i], w.G, q16s, scales, biases, Ys=Ys[i], workspace=wss[i], weights=descs[i])
+        calls()                      # warm-up outside the graph (configures the kernels)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            calls()
+        g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(replays):
+            g.replay()
+        b.record()
+        torch.cuda.synchronize()
+        status = ops.convrot_device_status()
+        if status != ops.OK:
+            raise ops.ConvrotError(status, "device status")
+        us = a.elapsed_time(b) * 1e3 / (replays * nsets)
+        out[name] = {"workload": f"X {'fp16' if name == 'unet' else 'fp32'} [{w.M},{w.K}] G={w.G} -> "
+                                 f"{len(w.Ns)} linear(s) N={list(w.Ns)}",
+                     "us_per_call": round(us, 3), "TOPS": round(w.gemm_ops / (us * 1e-6) / 1e12, 2),
+                     "calls_per_graph": nsets}
+        del Xs, Ys, wss, descs, g
+    return out
 
 
 def library_gemm_same_shape(w, dev, flush, ours_us, reps=20):
@@ -564,6 +621,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-library-gemm", dest="library_gemm", action="store_false",
                     help="skip timing cuBLAS on the GEMM's shape (context for the roofline)")
+    ap.add_argument("--no-small-configs", dest="small_configs", action="store_false",
+                    help="skip the tiny and UNet-like configs timed inside a CUDA graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
