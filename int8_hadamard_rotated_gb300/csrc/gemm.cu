@@ -71,9 +71,12 @@ static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
 static_assert(KB_PER_CHUNK * BK * 127 * 127 < (1 << 24), "chunk must stay exact in fp32");
 
 // Y staging for tensor-map stores: per epilogue warpgroup one buffer of
-// Y_ROWS activation rows x 128 output features (fp32).
-constexpr int Y_ROWS = 16;
-constexpr int Y_HALF_BYTES = Y_ROWS * CTA_M * 4;
+// Y_ROWS activation rows x 128 output features (fp32), two buffers per
+// epilogue warpgroup used in turn, so that filling one overlaps the store of
+// the other.
+constexpr int Y_ROWS = 8;
+constexpr int Y_BUF_BYTES = Y_ROWS * CTA_M * 4;
+constexpr int Y_HALF_BYTES = 2 * Y_BUF_BYTES;  // one warpgroup's two buffers
 
 template <int CG, int BN_, bool YTMA = false>
 struct Geom {
@@ -87,7 +90,7 @@ struct Geom {
   static constexpr int STAGES = (196 * 1024) / STAGE_BYTES;  // 4 (CG 1), 6-8 (pairs)
   static constexpr uint32_t IDESC = idesc_f16_f32(TILE_M, BN);
   // shared-memory layout (after aligning the base to 1024 B)
-  static constexpr int SMEM_YOUT = STAGES * STAGE_BYTES;                  // [2][Y_ROWS][128] fp32 (YTMA)
+  static constexpr int SMEM_YOUT = STAGES * STAGE_BYTES;                  // [2][2][Y_ROWS][128] fp32 (YTMA)
   static constexpr int SMEM_SX = SMEM_YOUT + (YTMA ? 2 * Y_HALF_BYTES : 0);  // [2][128] fp32 row scales (YTMA)
   static constexpr int SMEM_BARS = SMEM_SX + (YTMA ? 2 * 128 * 4 : 0);  // full[S], empty[S], tfull[2], tempty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 2 + 2 + 1;
@@ -100,6 +103,8 @@ static_assert(Geom<1, 256>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 256, true>::SMEM
                   Geom<2, 192, true>::SMEM_ALLOC <= 227 * 1024 && Geom<2, 128, true>::SMEM_ALLOC <= 227 * 1024,
               "shared memory");
 static_assert(2 * 256 <= TMEM_COLS, "two accumulators fit in TMEM");
+static_assert((256 / 2 / Y_ROWS) % 2 == 0 && (192 / 2 / Y_ROWS) % 2 == 0 && (128 / 2 / Y_ROWS) % 2 == 0,
+              "every tile height stores an even number of Y blocks per warpgroup");
 
 struct GemmParams {
   CUtensorMap tmap_x;              // activation codes, fp16 [M, K], box X_ROWS x 64
@@ -588,10 +593,10 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
         const float in_scale = UNSCALE ? p.in_scale[c.lin] : 1.0f;
         if (YTMA) {
-          // Y_ROWS rows at a time through this warpgroup's staging buffer and
-          // one tensor-map store (rows past M and features past N are not
-          // written by the store)
-          float* sy = reinterpret_cast<float*>(smem + Gm::SMEM_YOUT + half * Y_HALF_BYTES);
+          // Y_ROWS rows at a time through this warpgroup's two staging
+          // buffers in turn and one tensor-map store each (rows past M and
+          // features past N are not written by the store)
+          uint8_t* sy_base = smem + Gm::SMEM_YOUT + half * Y_HALF_BYTES;
           const bool store_leader = (quarter == 0 && lane == 0);
           const int col = 32 * quarter + lane;
           const int o_base = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
@@ -604,7 +609,11 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           if (col < COLS_PER_THREAD) ssx[col] = (r0 + col < p.M) ? __ldg(p.s_x + r0 + col) : 0.0f;
 #pragma unroll
           for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
-            if (store_leader) bulk_wait_read<0>();  // the previous store has read the buffer
+            // every block commits one bulk group (empty when nothing is
+            // stored) and the count of blocks per tile is even, so the group
+            // two back is the last store from this buffer: wait until it read it
+            float* sy = reinterpret_cast<float*>(sy_base + (sub & 1) * Y_BUF_BYTES);
+            if (store_leader) bulk_wait_read<1>();
             named_bar_sync(1 + half, 4 * 32);
 #pragma unroll
             for (int i = 0; i < Y_ROWS; i += 4) {
@@ -634,8 +643,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             }
             fence_proxy_async_smem();
             named_bar_sync(1 + half, 4 * 32);
-            if (store_leader && o_base < N && r0 + sub * Y_ROWS < p.M) {
-              tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
+            if (store_leader) {
+              if (o_base < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
               bulk_commit();
             }
           }
