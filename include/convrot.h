@@ -309,7 +309,9 @@ size_t convrot_linear_host_workspace_size(int64_t M, int64_t K, int x_dtype,
  * should be pinned (page-locked) for the transfers to overlap.
  *   X_host     [M,K] fp32/fp16 host array.
  *   weights    as convrot_linear; every Y is a host array [M,N_j] fp32.
- *   chunk_rows rows per chunk (0 = default 768; multiples of 256 suit the GEMM).
+ *   chunk_rows rows per chunk (0 = the default: a first chunk of 256 rows, so
+ *              that output copies start sooner, then chunks of 768; multiples
+ *              of 256 suit the GEMM).
  *   workspace  device scratch, >= convrot_linear_host_workspace_size(...).
  *   stream, copy_in_stream, copy_out_stream: cudaStream_t (NULL copy streams
  *              mean `stream`: correct but without overlap). The call is
