@@ -19,9 +19,10 @@
 // the int32 limit.
 //
 // Kernel shape. Persistent, one CTA per SM, 10 warps:
-//   warps 0-7  epilogue: drain TMEM chunks into int32 registers, reconstruct,
-//              store (each thread owns one output feature o and 128
-//              activation rows of a tile; a warp stores 128 B per row).
+//   warps 0-7  epilogue: drain TMEM chunks into registers, reconstruct, and
+//              store through shared memory with tensor-map stores (each
+//              thread owns one output feature o and 128 activation rows of a
+//              tile).
 //   warp 8     TMA producer: streams 64-deep K slices of the weight and
 //              activation binary16 codes (128-byte swizzle) into a ring of
 //              shared-memory stages.
@@ -37,8 +38,10 @@
 //     its "full" barrier; commits arrive on both CTAs' barriers.
 //   CG = 1: single CTAs, 128 weight rows x 256 activation rows per tile
 //     (48 KB, 4 stages); used where clusters cannot be launched.
-// Tiles of all linears sharing the input form one launch, walked in groups of
-// eight activation bands so weight tiles are reused from L2.
+// Tiles of all linears sharing the input form one launch, walked so that the
+// activation bands of a raster group stay in L2 while their weight tiles
+// stream through; a fractional last wave can be split by K (split waves), and
+// clusters of two pairs can share weight rows by multicast.
 #include "common.cuh"
 
 #include <cuda.h>
@@ -261,7 +264,7 @@ __device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, int
 }
 
 // K blocks (of BK) per exact fp32 chunk for a tile: the weight's plan for the
-// tile's 128-row blocks (their minimum), or KB_PER_CHUNK (1024 products,
+// tile's blocks of 128 weight rows (their minimum), or KB_PER_CHUNK (1024 products,
 // always exact) without a plan.
 template <int CG>
 __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoord& c) {
@@ -278,8 +281,8 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
 
 // UNSCALE: the variant for linears with an input scale other than 1 (the IEEE
 // division stays out of the common kernel's unrolled epilogue).
-// YTMA: Y leaves through shared memory and tensor-map stores (16 rows x 128
-// features per store) instead of per-thread global stores.
+// YTMA: Y leaves through shared memory and tensor-map stores (Y_ROWS rows x
+// 128 features per store) instead of per-thread global stores.
 // MC (with CG = 2): clusters of four CTAs, two pairs that work on the same
 // weight tile and two bands at once. Each CTA loads half of its 128 weight
 // rows and multicasts it to the CTA of the other pair that holds the same
