@@ -461,6 +461,9 @@ def run_gpu(args, rank, world, local_rank):
     del Xm, mlp_w, Ym, wsm
 
     library = library_gemm_same_shape(w, dev, flush, float(gemm_ms.mean() * 1e3)) if args.library_gemm else None
+    # context for "% INT8 TC peak": the legacy 8-bit integer tensor instruction's
+    # rate on this GPU (tcgen05 has no 8-bit integer kind here)
+    int8_rate = ops.convrot_probe_int8_mma_rate(20000)
     small = small_configs_in_graph(dev) if args.small_configs else None
 
     pack = {
@@ -488,6 +491,11 @@ def run_gpu(args, rank, world, local_rank):
                    "gemm_us_mean_alone": float(gemm_ms.mean() * 1e3), "wall_s_timed_loop": wall},
         "e2e_parity_max_abs_diff": float(max((a - b).abs().max().item() for a, b in zip(Yt, Y_host))),
     }
+    result["int8_mma_sync_probe"] = {
+        "TOPS": round(int8_rate, 1),
+        "what": "register-only mma.sync m16n8k32 s8 x s8 -> s32 on every SM (the only 8-bit integer tensor "
+                "instruction on sm_103a)",
+        "gemm_achieved_over_it": round(gemm_tflops / int8_rate, 3)}
     if library is not None:
         result["library_gemm_same_shape"] = library
     if small is not None:

@@ -423,6 +423,17 @@ int convrot_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, int
  */
 int convrot_device_status(void* stream);
 
+/*
+ * convrot_probe_int8_mma_rate -- a diagnostic, not part of the method: runs a
+ * register-only microbenchmark of the legacy 8-bit integer tensor instruction
+ * (mma.sync m16n8k32 s8 x s8 -> s32; sm_103a's tcgen05 has no 8-bit integer
+ * kind) on the current device and returns its rate in *tops (tera-ops per
+ * second, two ops per multiply-add). iters: rounds per warp (1e4 or so takes a
+ * few ms). Synchronous; allocates 4 bytes of device memory.
+ * Errors: ERR_ARG, ERR_DEVICE, ERR_CUDA.
+ */
+int convrot_probe_int8_mma_rate(int iters, double* tops);
+
 #ifdef __cplusplus
 }
 #endif

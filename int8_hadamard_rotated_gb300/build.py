@@ -23,7 +23,7 @@ BUILD_DIR = os.path.join(ROOT, "_build", "libconvrot")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libconvrot.so")
 
-SOURCES = ["api.cu", "pack.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu"]
+SOURCES = ["api.cu", "pack.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu", "probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE]

@@ -129,3 +129,11 @@ def test_empty_shapes(ops):
     Qx = torch.zeros((4, 64), dtype=torch.int8, device="cuda")
     A = ops.int8_gemm_s32(Qx, Q_w16=torch.zeros((0, 64), dtype=torch.float16, device="cuda"))
     assert A.shape == (4, 0)
+
+
+def test_int8_mma_rate_probe_runs(ops):
+    """The diagnostic microbenchmark of the legacy s8 tensor instruction runs
+    and reports a positive, finite rate."""
+    import math
+    tops = ops.convrot_probe_int8_mma_rate(2000)
+    assert math.isfinite(tops) and tops > 0.0
