@@ -125,3 +125,29 @@ def test_graph_replay_of_a_split_gemm(ops):
         for a, b in zip(got, want):
             np.testing.assert_array_equal(a, b)
     assert ops.convrot_device_status() == ops.OK
+
+
+def test_split_with_direct_stores_and_input_scale(ops):
+    """Split waves on the kernels without the staged Y stores: N not a
+    multiple of 4 (per-thread stores) and an input scale other than 1 (the
+    unscaling variant). Identical to whole tiles; the scaled linear also
+    matches the oracle."""
+    rng = workloads.rng_for(4608 + 3070)
+    M, K, G = 4608, 3072, 256
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0)
+    Ws = [workloads.weights(rng, 3070, K) for _ in range(3)]   # 18 bands x 12 weight tiles x 3 = 648 tiles
+    bs = [workloads.biases(rng, 3070) for _ in range(3)]
+    preps = [ops.convrot_prepare_weight(dev(W), G) for W in Ws]
+    q16s, scales, biases = [p[2] for p in preps], [p[1] for p in preps], [dev(b) for b in bs]
+    Q16, s16 = ops.convrot_pack_activations_f16(dev(X), G)
+    whole = [host(y) for y in ops.convrot_linear_packed(Q16, s16, q16s, scales, biases, split_tail=False)]
+    split = [host(y) for y in ops.convrot_linear_packed(Q16, s16, q16s, scales, biases)]
+    for a, b in zip(whole, split):
+        np.testing.assert_array_equal(a, b)
+    a = 0.37   # all three linears: 648 tiles, so the unscaling kernel splits its last waves too
+    Ys = ops.convrot_linear_scaled(dev(X), G, a, q16s, scales, biases)
+    from parity import assert_y
+    for j in range(3):
+        ref = oracle.linear_scaled(X[:512], host(preps[j][0]), host(preps[j][1]), bs[j], G, a)
+        assert_y(host(Ys[j])[:512], ref)
+    assert ops.convrot_device_status() == ops.OK
