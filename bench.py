@@ -460,6 +460,8 @@ def run_gpu(args, rank, world, local_rank):
            "ops_per_call": int(mw.gemm_ops)}
     del Xm, mlp_w, Ym, wsm
 
+    nxt = next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step)
+
     library = library_gemm_same_shape(w, dev, flush, float(gemm_ms.mean() * 1e3)) if args.library_gemm else None
     # context for "% INT8 TC peak": the legacy 8-bit integer tensor instruction's
     # rate on this GPU (tcgen05 has no 8-bit integer kind here)
@@ -484,7 +486,7 @@ def run_gpu(args, rank, world, local_rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "int8", "data": data_desc(w), "config": config_dict(w, world),
-        "roofline": roofline, "pack": pack, "mlp_chain": mlp, "e2e": e2e,
+        "roofline": roofline, "pack": pack, "mlp_chain": mlp, "next_rows": nxt, "e2e": e2e,
         "gpu_launches": 2 * args.steps,  # pack + grouped GEMM per timed step
         "clocks": clocks,
         "timing": {"step_ms_median": float(np.median(step_ms)), "pack_us_mean_alone": float(pack_ms.mean() * 1e3),
@@ -555,6 +557,83 @@ def small_configs_in_graph(dev, replays=5):
                      "calls_per_graph": nsets}
         del Xs, Ys, wss, descs, g
     return out
+
+
+def next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step, reps=20):
+    """Context for the rows beyond the step, each on the DiT input and timed
+    like the step's parts (L2 flushed before every launch, CUDA events on the
+    launching stream, mean over `reps`): the pack with the modulation prologue
+    (RMS norm, per-channel weight, (x + x*scale) + shift) beside the plain
+    pack of the same X; the one-call linear with an input scale beside the
+    plain one-call linear; the expansion of packed 4-bit weights of one
+    projection. Not part of the step."""
+    import torch
+    from int8_hadamard_rotated_gb300 import ops
+
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    L = ops.lib()
+    M, K = X.shape
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        ev = []
+        for _ in range(reps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3  # us
+
+    # f2: modulation prologue fused into the pack (int8 codes)
+    wv, sc, sh = (torch.from_numpy(v).to(dev) for v in workloads.modulation(workloads.rng_for(11), K))
+    Q = torch.empty((M, K), dtype=torch.int8, device=dev)
+    s = torch.empty((M,), dtype=torch.float32, device=dev)
+    t_pro = timed(lambda: ops.convrot_pack_prologue(X, w.G, rmsnorm=True, weight=wv, scale=sc, shift=sh,
+                                                    Q_x=Q, s_x=s, stream=stream))
+    t_plain = timed(lambda: ops.convrot_pack_activations(X, w.G, Q_x=Q, s_x=s, stream=stream))
+    pro_bytes = M * K * 4 + M * K + M * 4 + 3 * K * 4
+    f2 = {"workload": f"X fp32 [{M},{K}], G={w.G}: RMS norm, weight, (x + x*scale) + shift, then the pack -> int8 + s",
+          "bound": "hbm", "bytes": pro_bytes, "us": round(t_pro, 2),
+          "GB/s": round(pro_bytes / (t_pro * 1e-6) / 1e9, 1), "frac": round(pro_bytes / (t_pro * 1e-6) / 1e9 / hbm, 4),
+          "plain_pack_us": round(t_plain, 2)}
+    del Q, s
+
+    # f4: input scale (scaled pack, then the GEMM that unscales before the bias)
+    Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=dev) for q in q16s]
+    ws = torch.empty((ops.convrot_linear_workspace_size(M, K),), dtype=torch.uint8, device=dev)
+    wdesc = ops.make_weights(q16s, scales, biases, Ys, plans)
+    t_lin = timed(lambda: ops.convrot_linear(X, w.G, q16s, scales, biases, Ys=Ys, workspace=ws, stream=stream,
+                                             weights=wdesc))
+    t_scaled = timed(lambda: ops.convrot_linear_scaled(X, w.G, 0.37, q16s, scales, biases, Ys=Ys, workspace=ws,
+                                                       stream=stream, kchunks=plans))
+    f4 = {"workload": f"{w.name}: one convrot_linear_scaled call, input scale 0.37", "bound": "tensor",
+          "us": round(t_scaled, 2), "TOPS": round(ops_step / (t_scaled * 1e-6) / 1e12, 2),
+          "plain_linear_us": round(t_lin, 2), "plain_linear_TOPS": round(ops_step / (t_lin * 1e-6) / 1e12, 2)}
+    del Ys, ws
+
+    # f3: packed signed 4-bit weights of one projection -> int8 and binary16 codes (offline)
+    N = q16s[0].shape[0]
+    P = torch.from_numpy(workloads.packed_int4(workloads.rng_for(12), N, K)).to(dev)
+    q8 = torch.empty((N, K), dtype=torch.int8, device=dev)
+    q16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+
+    def expand():
+        st = L.convrot_w4_expand(P.data_ptr(), N, K, q8.data_ptr(), q16.data_ptr(), sp)
+        if st:
+            raise ops.ConvrotError(st, "convrot_w4_expand")
+    t_w4 = timed(expand)
+    w4_bytes = N * K // 2 + N * K + N * K * 2
+    f3 = {"workload": f"packed 4-bit W [{N},{K}] -> int8 + binary16 codes (offline; the GEMM is the step's)",
+          "bound": "hbm", "bytes": w4_bytes, "us": round(t_w4, 2),
+          "GB/s": round(w4_bytes / (t_w4 * 1e-6) / 1e9, 1), "frac": round(w4_bytes / (t_w4 * 1e-6) / 1e9 / hbm, 4)}
+    return {"f2_pack_prologue": f2, "f4_input_scale": f4, "f3_w4_expand": f3,
+            "note": "isolated launches, L2 flushed before each (launch latency included); "
+                    "frac against the measured HBM copy peak"}
 
 
 def library_gemm_same_shape(w, dev, flush, ours_us, reps=20):

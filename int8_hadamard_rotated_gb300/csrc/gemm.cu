@@ -622,8 +622,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             for (int i = 0; i < Y_ROWS; i += 4) {
               const int idx = sub * Y_ROWS + i;
               const float4 s4 = *reinterpret_cast<const float4*>(ssx + idx);
-              // float(A) * s_x * s_w + b, one rounding per operation, in that
-              // order, two rows at once
+              // float(A) * s_x * s_w (/ input scale) + b, one rounding per
+              // operation, in that order, two rows at once
               unsigned long long ya = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
                                                 pair_f32(s4.x, s4.y));
               unsigned long long yb = mul_f32x2(pair_f32(__int_as_float(acc[idx + 2]), __int_as_float(acc[idx + 3])),
@@ -631,6 +631,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
               if (sw_ptr) {
                 ya = mul_f32x2(ya, sw2);
                 yb = mul_f32x2(yb, sw2);
+              }
+              if (UNSCALE) {
+                // unscale before the bias (IEEE division, element by element)
+                float a0, a1, a2, a3;
+                unpair_f32(ya, a0, a1);
+                unpair_f32(yb, a2, a3);
+                ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
+                yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
               }
               if (b_ptr) {
                 ya = add_f32x2(ya, bb2);
@@ -1009,7 +1017,6 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
     unscale |= (lins[j].in_scale != 1.0f);
     ytma &= (lins[j].N % 4 == 0);  // tensor-map rows must be multiples of 16 bytes
   }
-  ytma &= !unscale;
   if (int st = configure_kernel<2, 256, false, true>()) return st;
   if (int st = configure_kernel<2, 192, false, true>()) return st;
   if (int st = configure_kernel<2, 128, false, true>()) return st;
@@ -1026,6 +1033,11 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
         if (ytma) return launch_pairs<256, false, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, quads, stream, sync);
         return launch_pairs<256, false, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, quads, stream, sync);
       }
+    }
+    if (ytma && unscale) {
+      if (bn == 128) return launch_pairs<128, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      if (bn == 192) return launch_pairs<192, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
+      return launch_pairs<256, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
     }
     if (ytma) {
       if (bn == 128) return launch_pairs<128, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);

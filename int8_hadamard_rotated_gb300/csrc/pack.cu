@@ -423,51 +423,67 @@ __device__ __forceinline__ void prologue_unit(float (&v)[16]) {
   }
 }
 
+// A row's sum of squares from the partial sums of its lane segments, stored
+// at part[0 .. nseg-1] by the segment leaders, added in segment order (so the
+// result does not depend on which segment finished first).
+__device__ __forceinline__ float row_sumsq(const float* part, int nseg) {
+  float tot = 0.0f;
+  for (int q = 0; q < nseg; ++q) tot += part[q];
+  return tot;
+}
+
 // 1 / sqrt(sum / K + eps) of a row from its sum of squares (IEEE fp32 steps).
 __device__ __forceinline__ float rms_factor(float sumsq, int K, float eps) {
   const float mean = __fdiv_rn(sumsq, static_cast<float>(K));
   return __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
 }
 
-// The per-channel part of the modulation prologue on unit u (elements
-// 16u .. 16u+15): x * r, then * weight, then (x + x * scale) + shift, each
-// operation one fp32 rounding; absent parts are skipped.
-__device__ __forceinline__ void modulate_unit(float (&v)[16], int u, float r, bool rms, const ModPrologue& m) {
+// The modulation vectors staged in shared memory: the 48 16-byte chunks a
+// thread at position t of its row uses (chunk c of unit slot j of vector k:
+// 0 weight, 1 scale, 2 shift) are consecutive from t * kModStride. The one
+// chunk of padding makes lanes t .. t+7 start 196 words apart, on distinct
+// banks, and every read is a per-thread base plus a constant offset.
+constexpr int kModStride = 49;
+__device__ __forceinline__ int mod_slot(int k, int j, int c) { return (k * 4 + j) * 4 + c; }
+
+// Chunk c (features 4c .. 4c+3 of unit u) of modulation vector k, from global memory.
+__device__ __forceinline__ float4 mod_chunk_global(const ModPrologue& m, int k, int u, int c) {
+  const float* base = (k == 0) ? m.weight : (k == 1) ? m.scale : m.shift;
+  return __ldg(reinterpret_cast<const float4*>(base + 16 * u) + c);
+}
+
+// The per-channel part of the modulation prologue on one unit: x * r, then
+// * weight, then (x + x * scale) + shift, each operation one fp32 rounding;
+// absent parts are skipped. chunk(k, c) gives the unit's chunk c of vector k.
+template <typename Chunk>
+__device__ __forceinline__ void modulate_unit(float (&v)[16], float r, bool rms, const ModPrologue& m, Chunk chunk) {
   if (rms) {
 #pragma unroll
     for (int p = 0; p < 16; ++p) v[p] = __fmul_rn(v[p], r);
   }
-  if (m.weight) {
-    const float4* w4 = reinterpret_cast<const float4*>(m.weight + 16 * u);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 w = __ldg(w4 + i);
-      v[4 * i] = __fmul_rn(v[4 * i], w.x);
-      v[4 * i + 1] = __fmul_rn(v[4 * i + 1], w.y);
-      v[4 * i + 2] = __fmul_rn(v[4 * i + 2], w.z);
-      v[4 * i + 3] = __fmul_rn(v[4 * i + 3], w.w);
+  for (int c = 0; c < 4; ++c) {
+    float* x = v + 4 * c;
+    if (m.weight) {
+      const float4 w = chunk(0, c);
+      x[0] = __fmul_rn(x[0], w.x);
+      x[1] = __fmul_rn(x[1], w.y);
+      x[2] = __fmul_rn(x[2], w.z);
+      x[3] = __fmul_rn(x[3], w.w);
     }
-  }
-  if (m.scale) {
-    const float4* s4 = reinterpret_cast<const float4*>(m.scale + 16 * u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 c = __ldg(s4 + i);
-      v[4 * i] = __fadd_rn(v[4 * i], __fmul_rn(v[4 * i], c.x));
-      v[4 * i + 1] = __fadd_rn(v[4 * i + 1], __fmul_rn(v[4 * i + 1], c.y));
-      v[4 * i + 2] = __fadd_rn(v[4 * i + 2], __fmul_rn(v[4 * i + 2], c.z));
-      v[4 * i + 3] = __fadd_rn(v[4 * i + 3], __fmul_rn(v[4 * i + 3], c.w));
+    if (m.scale) {
+      const float4 q = chunk(1, c);
+      x[0] = __fadd_rn(x[0], __fmul_rn(x[0], q.x));
+      x[1] = __fadd_rn(x[1], __fmul_rn(x[1], q.y));
+      x[2] = __fadd_rn(x[2], __fmul_rn(x[2], q.z));
+      x[3] = __fadd_rn(x[3], __fmul_rn(x[3], q.w));
     }
-  }
-  if (m.shift) {
-    const float4* h4 = reinterpret_cast<const float4*>(m.shift + 16 * u);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 h = __ldg(h4 + i);
-      v[4 * i] = __fadd_rn(v[4 * i], h.x);
-      v[4 * i + 1] = __fadd_rn(v[4 * i + 1], h.y);
-      v[4 * i + 2] = __fadd_rn(v[4 * i + 2], h.z);
-      v[4 * i + 3] = __fadd_rn(v[4 * i + 3], h.w);
+    if (m.shift) {
+      const float4 h = chunk(2, c);
+      x[0] = __fadd_rn(x[0], h.x);
+      x[1] = __fadd_rn(x[1], h.y);
+      x[2] = __fadd_rn(x[2], h.z);
+      x[3] = __fadd_rn(x[3], h.w);
     }
   }
 }
@@ -486,6 +502,10 @@ __device__ __forceinline__ float row_sumsq_part(const float (&v)[4][16], int seg
   return ss;
 }
 
+// Lane segments per row: a row's tpr threads form aligned segments of
+// gcd(tpr, 32) lanes.
+__host__ __device__ constexpr int row_segments(int tpr) { return tpr / ((tpr & -tpr) < 32 ? (tpr & -tpr) : 32); }
+
 // ---- pack_kernel: the general path (per-thread cp.async) ---------------------
 
 // One CTA handles `rpc` rows with `tpr` threads each per block, persistently.
@@ -499,7 +519,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
   constexpr int CH = 4 * CPU;  // 16-byte chunks per thread per stage
   extern __shared__ uint4 stage_buf[];  // [1 or 2][CH][blockDim.x]
   __shared__ unsigned long long s_amax[2][kMaxRowsPerCta];
-  __shared__ float s_sumsq[2][kMaxRowsPerCta];
+  __shared__ float s_sumsq[kMaxThreads];  // [rpc][segments per row]: partial sums of squares
 
   const int tid = threadIdx.x;
   const int nth = blockDim.x;
@@ -511,10 +531,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
   const bool in_cta_row = lr < rpc;
 
   pdl_launch_dependents();  // the next kernel may set itself up; it waits for this one before reading
-  for (int i = tid; i < 2 * kMaxRowsPerCta; i += nth) {
-    (&s_amax[0][0])[i] = 0ull;
-    (&s_sumsq[0][0])[i] = 0.0f;
-  }
+  for (int i = tid; i < 2 * kMaxRowsPerCta; i += nth) (&s_amax[0][0])[i] = 0ull;
 
   const uint32_t sbase = smem_u32(stage_buf);
   auto issue = [&](int64_t blk, int stage) {
@@ -577,16 +594,19 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     if (PRO == kProModulate) {
       float r = 1.0f;
       if (mod.rms) {
+        // one slot per lane segment (the previous block's reads ended before
+        // the barrier that follows its row maximum)
+        const int nseg = tpr / segw;
         const float ss = row_sumsq_part(v, segw);
-        if (in_cta_row && t == 0) s_sumsq[slot ^ 1][lr] = 0.0f;  // for the next block
-        if (active && (t % segw) == 0) atomicAdd(&s_sumsq[slot][lr], ss);
+        if (active && (t % segw) == 0) s_sumsq[lr * nseg + t / segw] = ss;
         __syncthreads();
-        r = rms_factor(s_sumsq[slot][in_cta_row ? lr : 0], K, mod.eps);
+        r = rms_factor(row_sumsq(s_sumsq + (in_cta_row ? lr : 0) * nseg, nseg), K, mod.eps);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int u = in_unit_grouped<G>(gi, li, j);
-        if (active && u < units) modulate_unit(v[j], u, r, mod.rms != 0, mod);
+        if (active && u < units)
+          modulate_unit(v[j], r, mod.rms != 0, mod, [&](int k, int c) { return mod_chunk_global(mod, k, u, c); });
       }
     }
     rotate64<G>(v, ls);
@@ -672,8 +692,10 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   uint8_t* in_base = smem;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(p.nstages) * p.stage_bytes);
   unsigned long long* s_amax = reinterpret_cast<unsigned long long*>(full + kTmaMaxStages);
+  // [R][segments per row]: partial sums of squares of the lane segments
   float* s_sumsq = reinterpret_cast<float*>(s_amax + 2 * p.R);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_sumsq + 2 * p.R);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(s_sumsq + p.R * row_segments(p.tpr));
+  float4* s_vec = reinterpret_cast<float4*>((reinterpret_cast<uintptr_t>(abort_flag) + 4 + 15) & ~uintptr_t(15));
   int* err = &g_pack_error;
 
   const int tid = threadIdx.x;
@@ -688,17 +710,33 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const bool in_cta_row = lr < R;
   const int lr_read = in_cta_row ? lr : 0;  // padding threads read row 0 and store nothing
   const int S = p.nstages;
+  float4* s_mod = s_vec + t * kModStride;  // kProModulate: this column's vector chunks
+
+  // units of this thread: round-robin over the row for G <= 16, the group's top
+  // digit for G >= 64
+  int u_of[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) u_of[j] = (G <= 16) ? t + tpr * j : in_unit_grouped<G>(gi, li, j);
 
   pdl_launch_dependents();  // the next kernel may set itself up; it waits for this one before reading
-  for (int i = tid; i < 2 * R; i += blockDim.x) {
-    s_amax[i] = 0ull;
-    s_sumsq[i] = 0.0f;
-  }
+  for (int i = tid; i < 2 * R; i += blockDim.x) s_amax[i] = 0ull;
   if (tid == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&full[s], 1);
     *abort_flag = 0;
     fence_mbarrier_init();
     tma_prefetch_desc(&p.tmap);
+  }
+  if (PRO == kProModulate && lr == 0) {
+    // the first row's threads stage the vector values of their units, once
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+      for (int k = 0; k < 3; ++k) {
+        const float* base = (k == 0) ? p.mod.weight : (k == 1) ? p.mod.scale : p.mod.shift;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          if (base && u_of[j] < units) s_mod[mod_slot(k, j, c)] = mod_chunk_global(p.mod, k, u_of[j], c);
+      }
   }
   __syncthreads();
 
@@ -726,11 +764,6 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
   const LaneSigns<G> ls = lane_signs<G>(li);
   const int seg = tpr & -tpr;
   const int segw = seg < 32 ? seg : 32;
-  // units of this thread: round-robin over the row for G <= 16, the group's top
-  // digit for G >= 64
-  int u_of[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) u_of[j] = (G <= 16) ? t + tpr * j : in_unit_grouped<G>(gi, li, j);
 
   const int64_t stride = gridDim.x;
   int64_t n_issued = 0;  // thread 0: blocks issued (block i of this CTA goes to stage i % S)
@@ -775,15 +808,19 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
     if (PRO == kProModulate) {
       float r = 1.0f;
       if (p.mod.rms) {
+        // one slot per lane segment (the previous block's reads ended before
+        // the barrier that follows its row maximum)
+        const int nseg = tpr / segw;
         const float ss = row_sumsq_part(v, segw);
-        if (in_cta_row && t == 0) s_sumsq[(slot ^ 1) * R + lr] = 0.0f;  // for the next block
-        if (active && (t % segw) == 0) atomicAdd(&s_sumsq[slot * R + lr], ss);
+        if (active && (t % segw) == 0) s_sumsq[lr * nseg + t / segw] = ss;
         __syncthreads();
-        r = rms_factor(s_sumsq[slot * R + lr_read], K, p.mod.eps);
+        r = rms_factor(row_sumsq(s_sumsq + lr_read * nseg, nseg), K, p.mod.eps);
       }
 #pragma unroll
       for (int j = 0; j < 4; ++j)
-        if (active && u_of[j] < units) modulate_unit(v[j], u_of[j], r, p.mod.rms != 0, p.mod);
+        if (active && u_of[j] < units)
+          modulate_unit(v[j], r, p.mod.rms != 0, p.mod,
+                        [&](int k, int c) { return s_mod[mod_slot(k, j, c)]; });
     }
     rotate64<G>(v, ls);
 
@@ -910,10 +947,20 @@ int launch_pack_cpasync(const void* X, int64_t M, int K, float in_scale, const M
 constexpr size_t kSmemPerCtaMax = 227 * 1024;
 constexpr uint32_t kTargetBlockBytes = 24 * 1024;  // input bytes of one block
 constexpr int kStages = 2;                          // blocks in flight per CTA
+constexpr int kVecSmemMaxK = 4096;                  // longest rows whose modulation vectors are staged
+// The modulated pack stages the modulation vectors once per CTA, so it takes
+// larger blocks (more rows share them) in fewer stages.
+constexpr uint32_t kModTargetBlockBytes = 48 * 1024;
+constexpr int kModStages = 1;
 
 // Shape of the TMA path for rows of K elements, or false when it does not apply.
+// `extra`: shared-memory bytes the kernel needs besides the stages and its
+// bookkeeping (the staged modulation vectors).
+// `block_target`, `max_stages`: the input bytes of one block and the blocks
+// in flight per CTA to aim for.
 template <typename TIn, int OUT>
-bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
+bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem, size_t extra = 0,
+              uint32_t block_target = kTargetBlockBytes, int max_stages = kStages) {
   constexpr int ESZ = static_cast<int>(sizeof(TIn));
   const int64_t row_in = static_cast<int64_t>(K) * ESZ;
   if (row_in % 128 != 0) return false;
@@ -922,7 +969,7 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
   if (tpr > kMaxThreads) return false;
   int R, Lb, rbox;
   if (L <= 256) {
-    R = static_cast<int>(kTargetBlockBytes / row_in);
+    R = static_cast<int>(block_target / row_in);
     R = std::max(1, std::min(R, std::min(256, kMaxThreads / tpr)));
     Lb = L;
     rbox = R;
@@ -938,8 +985,8 @@ bool plan_tma(int K, PackTmaParams& p, int& threads, size_t& smem) {
     rbox = 1;
   }
   const uint32_t stage_bytes = static_cast<uint32_t>(((static_cast<int64_t>(R) * L * 128 + 1023) / 1024) * 1024);
-  const size_t misc = 1024 + kTmaMaxStages * 8 + 2 * static_cast<size_t>(R) * 12 + 16;
-  int S = kStages;
+  const size_t misc = 1024 + kTmaMaxStages * 8 + static_cast<size_t>(R) * (16 + 4 * row_segments(tpr)) + 16 + extra;
+  int S = max_stages;
   while (S > 1 && misc + static_cast<size_t>(S) * stage_bytes > kSmemPerCtaMax) --S;
   smem = misc + static_cast<size_t>(S) * stage_bytes;
   if (smem > kSmemPerCtaMax) return false;
@@ -962,7 +1009,15 @@ int launch_pack_t(const void* X, int64_t M, int K, float in_scale, const ModProl
   memset(&p, 0, sizeof(p));
   int threads = 0;
   size_t smem = 0;
-  if (!plan_tma<TIn, OUT>(K, p, threads, smem))
+  // the modulated pack keeps the modulation vectors in shared memory (48
+  // 16-byte chunks and one of padding per thread of a row); rows longer than kVecSmemMaxK
+  // features take the general kernel, which reads them from global memory
+  if (PRO == kProModulate && K > kVecSmemMaxK)
+    return launch_pack_cpasync<G, TIn, OUT, PRO>(X, M, K, in_scale, mod, out, scales, stream);
+  const bool modulated = (PRO == kProModulate);
+  const size_t extra = modulated ? static_cast<size_t>(kModStride * 16) * ((K + 63) / 64) + 16 : 0;
+  if (!plan_tma<TIn, OUT>(K, p, threads, smem, extra, modulated ? kModTargetBlockBytes : kTargetBlockBytes,
+                          modulated ? kModStages : kStages))
     return launch_pack_cpasync<G, TIn, OUT, PRO>(X, M, K, in_scale, mod, out, scales, stream);
 
   EncodeTiledFn enc = get_encode_fn();

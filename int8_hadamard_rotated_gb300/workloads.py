@@ -153,6 +153,20 @@ def make_case(w: Workload, *, M: Optional[int] = None) -> Case:
     return Case(X=X, Ws=Ws, bs=bs)
 
 
+def modulation(rng: np.random.Generator, K: int):
+    """Per-channel vectors of the pack's modulation prologue: a norm weight
+    ~ 1 + N(0, 0.1), a modulation scale ~ N(0, 0.2) and shift ~ N(0, 0.05)."""
+    w = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)
+    sc = (0.2 * rng.standard_normal(K)).astype(np.float32)
+    sh = (0.05 * rng.standard_normal(K)).astype(np.float32)
+    return w, sc, sh
+
+
+def packed_int4(rng: np.random.Generator, N: int, K: int) -> np.ndarray:
+    """Uniform random bytes [N, K/2]: two signed 4-bit weights each."""
+    return rng.integers(0, 256, size=(N, K // 2), dtype=np.int64).astype(np.uint8)
+
+
 def random_codes(rng: np.random.Generator, rows: int, cols: int,
                  low: int = -127, high: int = 127) -> np.ndarray:
     """Uniform int8 codes in [low, high] (for GEMM-only cases)."""

@@ -181,3 +181,28 @@ def test_input_scale(ops, a):
     if a in (1.0, 0.25):
         (Y1,) = ops.convrot_linear(dev(case.X), G, [Qw16], [s_w], [dev(case.bs[0])])
         np.testing.assert_array_equal(Y, host(Y1))
+
+
+def test_input_scale_epilogue_bit_exact(ops):
+    """The scaled linear on the DiT projections (staged Y stores, split
+    waves) equals, bit for bit, the reconstruction formed on the host in fp32
+    from the raw int32 product of the codes it packed:
+    ((float(A) * s_x) * s_w) / a + b, one rounding per operation, in that
+    order."""
+    w = workloads.get("dit_qkv")
+    case = workloads.make_case(w)
+    M, K, G, a = w.M, w.K, w.G, np.float32(0.37)
+    preps = [ops.convrot_prepare_weight(dev(W), G) for W in case.Ws]
+    q16s, scales = [p[2] for p in preps], [p[1] for p in preps]
+    biases = [dev(b) for b in case.bs]
+    ws = torch.empty((ops.convrot_linear_workspace_size(M, K),), dtype=torch.uint8, device="cuda")
+    Ys = ops.convrot_linear_scaled(dev(case.X), G, float(a), q16s, scales, biases, workspace=ws)
+    Q8 = ws[: M * K * 2].view(torch.float16).view(M, K).to(torch.int8)
+    off = (M * K * 2 + 255) // 256 * 256
+    s_x = host(ws[off: off + 4 * M].view(torch.float32))
+    for j in range(3):
+        A = host(ops.int8_gemm_s32(Q8, Q_w16=q16s[j]))
+        ref = (A.astype(np.float32) * s_x[:, None]) * host(scales[j])[None, :]
+        ref = ref / a + case.bs[j][None, :]
+        np.testing.assert_array_equal(host(Ys[j]), ref)
+    assert ops.convrot_device_status() == ops.OK

@@ -14,11 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 def vectors(seed, K):
-    rng = workloads.rng_for(seed)
-    w = (1.0 + 0.1 * rng.standard_normal(K)).astype(np.float32)
-    sc = (0.2 * rng.standard_normal(K)).astype(np.float32)
-    sh = (0.05 * rng.standard_normal(K)).astype(np.float32)
-    return w, sc, sh
+    return workloads.modulation(workloads.rng_for(seed), K)
 
 
 @pytest.mark.parametrize("M,K,G", [(4608, 3072, 256), (37, 1280, 64), (9, 48, 4), (130, 12288, 1024)])
@@ -52,3 +48,19 @@ def test_linear_prologue(ops):
     Xp = oracle.prologue(case.X, rmsnorm=True, eps=1e-6, weight=g, scale=sc, shift=sh)
     for y, p, b in zip(Ys, preps, case.bs[:2]):
         assert_y(host(y), oracle.linear(Xp, host(p[0]), host(p[1]), b, w.G))
+
+
+@pytest.mark.parametrize("M,K", [(4608, 3072), (300, 12288)])
+def test_modulated_pack_is_repeatable(ops, M, K):
+    """The RMS norm's row sum of squares is added in a fixed order of its lane
+    segments, so repeated packs of one input are bit-identical (on the
+    TMA-fed kernel, and on the general kernel that long rows take)."""
+    rng = workloads.rng_for(M + K + 5)
+    X = dev(workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0))
+    w, sc, sh = (dev(v) for v in vectors(M + K, K))
+    runs = [ops.convrot_pack_prologue(X, 256, rmsnorm=True, weight=w, scale=sc, shift=sh) for _ in range(3)]
+    Q0, s0 = host(runs[0][0]), host(runs[0][1])
+    for Q, s in runs[1:]:
+        np.testing.assert_array_equal(host(Q), Q0)
+        np.testing.assert_array_equal(host(s), s0)
+    assert ops.convrot_device_status() == ops.OK

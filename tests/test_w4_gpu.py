@@ -13,8 +13,7 @@ pytestmark = pytest.mark.gpu
 
 
 def packed_weights(seed, N, K):
-    rng = workloads.rng_for(seed)
-    return rng.integers(0, 256, size=(N, K // 2), dtype=np.int64).astype(np.uint8)
+    return workloads.packed_int4(workloads.rng_for(seed), N, K)
 
 
 @pytest.mark.parametrize("N,K", [(1, 16), (300, 3072), (129, 1280)])
