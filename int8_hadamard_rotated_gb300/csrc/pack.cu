@@ -453,38 +453,37 @@ __device__ __forceinline__ float4 mod_chunk_global(const ModPrologue& m, int k, 
 }
 
 // The per-channel part of the modulation prologue on one unit: x * r, then
-// * weight, then (x + x * scale) + shift, each operation one fp32 rounding;
-// absent parts are skipped. chunk(k, c) gives the unit's chunk c of vector k.
+// * weight, then (x + x * scale) + shift, each operation one fp32 rounding
+// (lane-wise pairs, each lane rounded as the scalar operation); absent parts
+// are skipped. chunk(k, c) gives the unit's chunk c of vector k.
 template <typename Chunk>
 __device__ __forceinline__ void modulate_unit(float (&v)[16], float r, bool rms, const ModPrologue& m, Chunk chunk) {
-  if (rms) {
-#pragma unroll
-    for (int p = 0; p < 16; ++p) v[p] = __fmul_rn(v[p], r);
-  }
+  const unsigned long long r2 = f2pack(r, r);
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
-    float* x = v + 4 * c;
+    unsigned long long lo = f2pack(v[4 * c], v[4 * c + 1]);
+    unsigned long long hi = f2pack(v[4 * c + 2], v[4 * c + 3]);
+    if (rms) {
+      lo = mul2(lo, r2);
+      hi = mul2(hi, r2);
+    }
     if (m.weight) {
       const float4 w = chunk(0, c);
-      x[0] = __fmul_rn(x[0], w.x);
-      x[1] = __fmul_rn(x[1], w.y);
-      x[2] = __fmul_rn(x[2], w.z);
-      x[3] = __fmul_rn(x[3], w.w);
+      lo = mul2(lo, f2pack(w.x, w.y));
+      hi = mul2(hi, f2pack(w.z, w.w));
     }
     if (m.scale) {
       const float4 q = chunk(1, c);
-      x[0] = __fadd_rn(x[0], __fmul_rn(x[0], q.x));
-      x[1] = __fadd_rn(x[1], __fmul_rn(x[1], q.y));
-      x[2] = __fadd_rn(x[2], __fmul_rn(x[2], q.z));
-      x[3] = __fadd_rn(x[3], __fmul_rn(x[3], q.w));
+      lo = add2(lo, mul2(lo, f2pack(q.x, q.y)));
+      hi = add2(hi, mul2(hi, f2pack(q.z, q.w)));
     }
     if (m.shift) {
       const float4 h = chunk(2, c);
-      x[0] = __fadd_rn(x[0], h.x);
-      x[1] = __fadd_rn(x[1], h.y);
-      x[2] = __fadd_rn(x[2], h.z);
-      x[3] = __fadd_rn(x[3], h.w);
+      lo = add2(lo, f2pack(h.x, h.y));
+      hi = add2(hi, f2pack(h.z, h.w));
     }
+    f2unpack(lo, v[4 * c], v[4 * c + 1]);
+    f2unpack(hi, v[4 * c + 2], v[4 * c + 3]);
   }
 }
 
