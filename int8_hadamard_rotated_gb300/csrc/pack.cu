@@ -48,6 +48,11 @@
 //   pack_kernel (any K % 16 == 0, rows up to 32768 elements): per-thread
 //     16-byte cp.async copies into a lane-interleaved two-stage buffer and
 //     direct 16-byte stores of the codes.
+// An elementwise prologue may transform each loaded row first: GELU, or the
+// modulation (RMS norm, per-channel weight, (x + x*scale) + shift). The
+// modulated pack takes pack_tma_kernel for rows of up to kVecSmemMaxK
+// features, with the three modulation vectors staged once per CTA in shared
+// memory, and pack_kernel for longer rows.
 #include "common.cuh"
 
 #include <algorithm>
@@ -676,7 +681,9 @@ struct PackTmaParams {
 //                           it (natural layout) and bulk-copied out
 //   [kTmaMaxStages] u64     "stage full" barriers
 //   [2][R] u64              tagged row absmax
+//   [R][segments] f32       partial sums of squares (RMS norm)
 //   int                     abort flag
+//   [tpr][kModStride] 16 B  modulation vector chunks (kProModulate; 16-byte aligned)
 template <int G, typename TIn, int OUT, int PRO>
 __global__ void __launch_bounds__(kMaxThreads)
 pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
