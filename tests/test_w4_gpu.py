@@ -16,7 +16,7 @@ def packed_weights(seed, N, K):
     return workloads.packed_int4(workloads.rng_for(seed), N, K)
 
 
-@pytest.mark.parametrize("N,K", [(1, 16), (300, 3072), (129, 1280)])
+@pytest.mark.parametrize("N,K", [(1, 16), (3, 48), (300, 3072), (129, 1280)])  # (1, 16), (3, 48): odd pack counts
 def test_w4_expand_matches_unpack(ops, N, K):
     P = packed_weights(N + K, N, K)
     q8, q16 = ops.convrot_w4_expand(dev(P), K)
