@@ -184,6 +184,60 @@ def source_hash():
         return hashlib.sha256(f.read()).hexdigest()
 
 
+def bench_lib():
+    """The benchmark's own measurement kernels (libconvrot_bench.so, built
+    beside libconvrot.so): a size-matched streaming copy and a probe of the
+    legacy s8 tensor instruction. Neither is part of the library."""
+    import ctypes
+    from int8_hadamard_rotated_gb300 import build
+    L = ctypes.CDLL(build.BENCH_LIB_PATH)
+    L.bench_probe_int8_mma_rate.restype = ctypes.c_int
+    L.bench_probe_int8_mma_rate.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    L.bench_copy_ceiling.restype = ctypes.c_int
+    L.bench_copy_ceiling.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int,
+                                     ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p]
+    return L
+
+
+def int8_mma_rate(iters=20000):
+    """TOPS of the legacy mma.sync s8 instruction on the current device."""
+    import ctypes
+    out = ctypes.c_double(0.0)
+    st = bench_lib().bench_probe_int8_mma_rate(int(iters), ctypes.byref(out))
+    if st != 0:
+        raise RuntimeError(f"bench_probe_int8_mma_rate failed: {st}")
+    return float(out.value)
+
+
+def copy_ceiling_us(X, out_bytes, flush, stream, reps=20, ctas_per_sm=8):
+    """Mean time of the size-matched copy of X fp32 [M, K] -> out_bytes per
+    element + one fp32 word per row, L2 flushed before each launch like the
+    pack it is the ceiling for."""
+    import torch
+    M, K = X.shape
+    out = torch.empty((M, K * out_bytes), dtype=torch.uint8, device=X.device)
+    sc = torch.empty((M,), dtype=torch.float32, device=X.device)
+    L = bench_lib()
+
+    def run():
+        st = L.bench_copy_ceiling(X.data_ptr(), M, K, out_bytes, out.data_ptr(), sc.data_ptr(), ctas_per_sm,
+                                  stream.cuda_stream)
+        if st != 0:
+            raise RuntimeError(f"bench_copy_ceiling failed: {st}")
+    for _ in range(3):
+        run()
+    ev = []
+    for _ in range(reps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        run()
+        b.record(stream)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3
+
+
 def max_over_ranks(x: float, world: int, device=None) -> float:
     """The largest value over the ranks (the slowest rank's time); x itself
     with one rank. Every rank must call it (a collective)."""
@@ -301,7 +355,11 @@ def run_gpu(args, rank, world, local_rank):
     gemm_tflops = ops_step / (gemm_ms.mean() * 1e-3) / 1e12
     peak_tf = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
-    fused_pack_bytes = w.M * w.K * 4 + w.M * w.K * 2 + w.M * 4
+    # the pack's algorithmic bytes: fp32 X in, one int8 code per element and
+    # one fp32 scale per row out; the step's pack writes its codes as
+    # binary16 (the GEMM's operand), so it moves M*K more bytes than that
+    fused_pack_bytes = w.M * w.K * 4 + w.M * w.K + w.M * 4
+    fused_pack_moved = w.M * w.K * 4 + w.M * w.K * 2 + w.M * 4
     roofline = {
         "bound": "tensor", "kernel": "convrot_gemm_kernel (tcgen05 kind::f16, exact int32)",
         "achieved": round(gemm_tflops, 2), "peak": peak_tf, "unit": "TFLOP/s",
@@ -465,19 +523,35 @@ def run_gpu(args, rank, world, local_rank):
     library = library_gemm_same_shape(w, dev, flush, float(gemm_ms.mean() * 1e3)) if args.library_gemm else None
     # context for "% INT8 TC peak": the legacy 8-bit integer tensor instruction's
     # rate on this GPU (tcgen05 has no 8-bit integer kind here)
-    int8_rate = ops.convrot_probe_int8_mma_rate(20000)
+    int8_rate = int8_mma_rate(20000)
     small = small_configs_in_graph(dev) if args.small_configs else None
 
+    # the size-matched copies: the same bytes as the packs, no arithmetic
+    cc_sweep = copy_ceiling_us(Xp, 1, flush, stream)
+    cc_step = copy_ceiling_us(X, 2, flush, stream)
+    pack_us = float(pack_ms.mean()) * 1e3
     pack = {
         "workload": f"pack_sweep: X fp32 [{pw.M},{pw.K}] 0.5% channel outliers x30 -> int8 + s",
         "bytes_per_launch": pack_bytes, "bound": "hbm", "peak": hbm, "unit": "GB/s",
         "peak_kind": f"{peak_kind} HBM copy", "by_group": sweep,
         "by_group_note": "us/GB/s/frac: isolated launches, L2 flushed before each (launch latency included); "
                          "back_to_back: consecutive launches over rotating buffers larger than 4x L2",
-        "fused_step_pack": {"us": round(float(pack_ms.mean()) * 1e3, 2),
+        "copy_ceiling": {"what": "size-matched streaming copy (fp32 in, 1 B per element + 4 B per row out), "
+                                 "same flush protocol, no pack arithmetic",
+                         "us": round(cc_sweep, 2), "GB/s": round(pack_bytes / (cc_sweep * 1e-6) / 1e9, 1),
+                         "frac": round(pack_bytes / (cc_sweep * 1e-6) / 1e9 / hbm, 4)},
+        "fused_step_pack": {"us": round(pack_us, 2),
                             "bytes": fused_pack_bytes,
-                            "GB/s": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9, 1),
-                            "frac": round(fused_pack_bytes / (pack_ms.mean() * 1e-3) / 1e9 / hbm, 4)},
+                            "bytes_note": "algorithmic: fp32 X in, int8 codes + fp32 row scales out",
+                            "GB/s": round(fused_pack_bytes / (pack_us * 1e-6) / 1e9, 1),
+                            "frac": round(fused_pack_bytes / (pack_us * 1e-6) / 1e9 / hbm, 4),
+                            "bytes_moved": fused_pack_moved,
+                            "moved_note": "the codes are written as binary16, the GEMM's operand",
+                            "frac_moved": round(fused_pack_moved / (pack_us * 1e-6) / 1e9 / hbm, 4),
+                            "copy_ceiling_us": round(cc_step, 2),
+                            "copy_ceiling_note": "size-matched copy of the moved bytes (fp32 in, 2 B per "
+                                                 "element + 4 B per row out), same flush protocol",
+                            "frac_of_copy_ceiling": round(cc_step / pack_us, 4)},
         "long_rows": large,
     }
 

@@ -404,10 +404,12 @@ int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int G_up,
  *   of 256), e.g. M = 4608, K = 3072 fits; larger calls return
  *   CONVROT_ERR_SCRATCH without launching anything.
  * The call allocates nothing. Its first call on a device looks up the array's
- * device address (cudaGetSymbolAddress), so make that first call before any
- * stream capture. Every call on a device shares the one array: calls that
- * overlap on the GPU (different streams, or host threads sharing a device)
- * race and must be serialized by the caller.
+ * device address (cudaGetSymbolAddress) and remembers it with the identity of
+ * the current CUDA context; a call in another context (e.g. after
+ * cudaDeviceReset) looks it up again. Make the first call on a device, and
+ * the first after a reset, before any stream capture. Every call on a device
+ * shares the one array: calls that overlap on the GPU (different streams, or
+ * host threads sharing a device) race and must be serialized by the caller.
  * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_UNSUPPORTED,
  *         ERR_SCRATCH, ERR_CUDA.
  */
@@ -422,17 +424,6 @@ int convrot_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, int
  * (the kernel then skipped its remaining work and released its resources).
  */
 int convrot_device_status(void* stream);
-
-/*
- * convrot_probe_int8_mma_rate -- a diagnostic, not part of the method: runs a
- * register-only microbenchmark of the legacy 8-bit integer tensor instruction
- * (mma.sync m16n8k32 s8 x s8 -> s32; sm_103a's tcgen05 has no 8-bit integer
- * kind) on the current device and returns its rate in *tops (tera-ops per
- * second, two ops per multiply-add). iters: rounds per warp (1e4 or so takes a
- * few ms). Synchronous; allocates 4 bytes of device memory.
- * Errors: ERR_ARG, ERR_DEVICE, ERR_CUDA.
- */
-int convrot_probe_int8_mma_rate(int iters, double* tops);
 
 #ifdef __cplusplus
 }

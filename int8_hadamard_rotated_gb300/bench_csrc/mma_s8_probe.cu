@@ -1,11 +1,13 @@
-// probe.cu -- a microbenchmark of the legacy 8-bit integer tensor path
-// (mma.sync m16n8k32 s8 x s8 -> s32) on this GPU, as context for the GEMM's
-// roofline: sm_103a's tcgen05 tensor cores have no 8-bit integer kind, so the
-// exact INT8 product runs on binary16 operands; this measures what the only
-// INT8 tensor instruction left would deliver. Not part of the method.
-#include "common.cuh"
+// mma_s8_probe.cu -- a microbenchmark of the legacy 8-bit integer tensor path
+// (mma.sync m16n8k32 s8 x s8 -> s32), built into the benchmark's own small
+// library (libconvrot_bench.so), not into libconvrot.so. It gives the GEMM's
+// roofline its context: sm_103a's tcgen05 tensor cores have no 8-bit integer
+// kind, so the exact INT8 product runs on binary16 operands; this measures
+// what the only INT8 tensor instruction left would deliver. Not part of the
+// method.
+#include <cstdint>
+#include <cuda_runtime.h>
 
-namespace convrot {
 namespace {
 
 constexpr int kProbeThreads = 256;
@@ -43,31 +45,34 @@ __global__ void __launch_bounds__(kProbeThreads) mma_s8_probe_kernel(int iters, 
 }
 
 }  // namespace
-}  // namespace convrot
 
-using namespace convrot;
-
-extern "C" int convrot_probe_int8_mma_rate(int iters, double* tops) {
-  if (iters <= 0 || !tops) return CONVROT_ERR_ARG;
-  if (int st = check_device()) return st;
+// Returns 0 and the rate in *tops (tera-ops per second, two per multiply-add),
+// 1 for bad arguments, 2 if the current device is not sm_103, or 3 + the
+// cudaError_t of a failed CUDA call. Synchronous; allocates 4 bytes.
+extern "C" int bench_probe_int8_mma_rate(int iters, double* tops) {
+  if (iters <= 0 || !tops) return 1;
+  int dev = 0;
+  cudaDeviceProp prop;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return 3;
+  if (prop.major != 10 || prop.minor != 3) return 2;
   int* sink = nullptr;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
-  int st = CONVROT_OK;
-  const int blocks = device_sm_count() * 4;
+  int st = 0;
+  const int blocks = prop.multiProcessorCount * 4;
   float ms = 0.0f;
   if (cudaMalloc(&sink, sizeof(int)) != cudaSuccess || cudaEventCreate(&e0) != cudaSuccess ||
       cudaEventCreate(&e1) != cudaSuccess) {
-    st = set_cuda_error(cudaGetLastError());
+    st = 3 + static_cast<int>(cudaGetLastError());
   } else {
     mma_s8_probe_kernel<<<blocks, kProbeThreads>>>(iters / 10 + 1, sink);  // warm-up
     cudaEventRecord(e0);
     mma_s8_probe_kernel<<<blocks, kProbeThreads>>>(iters, sink);
     cudaEventRecord(e1);
     const cudaError_t e = cudaEventSynchronize(e1);
-    if (e != cudaSuccess) st = set_cuda_error(e);
-    else if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.0f) st = set_cuda_error(cudaErrorUnknown);
+    if (e != cudaSuccess) st = 3 + static_cast<int>(e);
+    else if (cudaEventElapsedTime(&ms, e0, e1) != cudaSuccess || ms <= 0.0f) st = 3 + static_cast<int>(cudaErrorUnknown);
   }
-  if (st == CONVROT_OK) {
+  if (st == 0) {
     const double ops = 2.0 * 16 * 8 * 32 * kProbeChains * static_cast<double>(iters) * blocks * (kProbeThreads / 32);
     *tops = ops / (ms * 1e-3) / 1e12;
   }

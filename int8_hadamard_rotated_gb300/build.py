@@ -2,7 +2,10 @@
 
 Each CUDA source is compiled in parallel with nvcc for sm_103a only, then the
 objects are linked into ``int8_hadamard_rotated_gb300/_lib/libconvrot.so``.
-Rebuilds are skipped when the library is newer than every source.
+The benchmark's own measurement kernels (a size-matched copy and a probe of
+the legacy s8 tensor instruction) go into a separate small library,
+``_lib/libconvrot_bench.so``, which the product never loads.
+Rebuilds are skipped when the libraries are newer than every source.
 
     python -m int8_hadamard_rotated_gb300.build [--force] [--verbose]
 """
@@ -22,8 +25,11 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build", "libconvrot")
 LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libconvrot.so")
+BENCH_LIB_PATH = os.path.join(LIB_DIR, "libconvrot_bench.so")
 
-SOURCES = ["api.cu", "pack.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu", "probe.cu"]
+SOURCES = ["api.cu", "pack.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu"]
+BENCH_CSRC = os.path.join(PKG, "bench_csrc")
+BENCH_SOURCES = ["copy_ceiling.cu", "mma_s8_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
               "--expt-relaxed-constexpr", "-I" + INCLUDE]
@@ -42,15 +48,16 @@ def nvcc_path() -> str:
 
 def _deps():
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files += [os.path.join(BENCH_CSRC, f) for f in os.listdir(BENCH_CSRC)]
     files.append(os.path.join(INCLUDE, "convrot.h"))
     files.append(os.path.abspath(__file__))
     return files
 
 
 def up_to_date() -> bool:
-    if not os.path.exists(LIB_PATH):
+    if not (os.path.exists(LIB_PATH) and os.path.exists(BENCH_LIB_PATH)):
         return False
-    t = os.path.getmtime(LIB_PATH)
+    t = min(os.path.getmtime(LIB_PATH), os.path.getmtime(BENCH_LIB_PATH))
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
@@ -62,30 +69,33 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     os.makedirs(BUILD_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
 
-    def compile_one(src):
+    def compile_one(job):
+        src_dir, src = job
         obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(CSRC, src), "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", os.path.join(src_dir, src), "-o", obj]
         if ptxas_info:
             cmd += ["-Xptxas", "-v"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
 
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        results = list(ex.map(compile_one, SOURCES))
-    objs = []
+    jobs = [(CSRC, s) for s in SOURCES] + [(BENCH_CSRC, s) for s in BENCH_SOURCES]
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(compile_one, jobs))
+    objs = {}
     for src, obj, r in results:
         if verbose or ptxas_info or r.returncode != 0:
             sys.stderr.write(f"== {src}\n{r.stdout}{r.stderr}")
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}")
-        objs.append(obj)
-    tmp = LIB_PATH + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", *objs, "-o", tmp]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    if r.returncode != 0:
-        sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("link of libconvrot.so failed")
-    os.replace(tmp, LIB_PATH)
+        objs[src] = obj
+    for path, srcs in ((LIB_PATH, SOURCES), (BENCH_LIB_PATH, BENCH_SOURCES)):
+        tmp = path + ".tmp"
+        cmd = [nvcc, *ARCH, "-shared", *[objs[s] for s in srcs], "-o", tmp]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            sys.stderr.write(r.stdout + r.stderr)
+            raise RuntimeError(f"link of {os.path.basename(path)} failed")
+        os.replace(tmp, path)
     return LIB_PATH
 
 

@@ -257,20 +257,6 @@ __device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const void* tma
       : "memory");
 }
 
-// 2-D tiled load for CTA-pair MMAs, multicast to the CTAs of `cta_mask` (the
-// same shared-memory offset in each). bar_cluster_addr is the barrier in this
-// CTA's pair leader (the even CTA of its pair); the bytes landing in each
-// destination are counted on the barrier at the same offset in the even CTA
-// of that destination's pair.
-__device__ __forceinline__ void tma_load_2d_pair_mc(void* smem_dst, const void* tmap, uint32_t bar_cluster_addr,
-                                                    int32_t x, int32_t y, uint16_t cta_mask, uint64_t cache_hint) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;"
-      ::"r"(smem_u32(smem_dst)), "l"(tmap), "r"(x), "r"(y), "r"(bar_cluster_addr), "h"(cta_mask), "l"(cache_hint)
-      : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory and the 5th-generation MMA
 // ---------------------------------------------------------------------------

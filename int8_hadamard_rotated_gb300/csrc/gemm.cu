@@ -40,8 +40,7 @@
 //     (48 KB, 4 stages); used where clusters cannot be launched.
 // Tiles of all linears sharing the input form one launch, walked so that the
 // activation bands of a raster group stay in L2 while their weight tiles
-// stream through; a fractional last wave can be split by K (split waves), and
-// clusters of two pairs can share weight rows by multicast.
+// stream through; a fractional last wave can be split by K (split waves).
 #include "common.cuh"
 
 #include <cuda.h>
@@ -125,11 +124,9 @@ struct GemmParams {
   int K;
   int num_kb;                      // ceil(K / BK)
   int n_xtiles;                    // ceil(M / BN) activation bands
-  int xgroup;                      // bands per unit of work: 1, or 2 (the two pairs of a cluster of four)
-  int n_xunits;                    // ceil(n_xtiles / xgroup)
   int n_wtiles;                    // sum over linears of ceil(N_j / TILE_M)
-  int total_tiles;                 // units of work: n_xunits * n_wtiles
-  int raster_bands;                // band units per raster group
+  int total_tiles;                 // n_xtiles * n_wtiles
+  int raster_bands;                // bands per raster group
   int n_lin;
   int raw_s32;
   // Balanced waves: the K blocks of the first sk_tiles tiles (0 = none) are
@@ -243,18 +240,15 @@ __device__ __forceinline__ bool wait_flag(const unsigned long long* flag, unsign
 // tile before moving to the next weight tile (of the same or the next
 // linear). The group's activation codes then stay in L2 while its weight
 // tiles stream through once.
-// With xgroup = 2 a unit of work is two tiles of one weight tile, on bands
-// 2u and 2u + 1; `pair` picks one (a band past the last one is a tile of
-// zero-filled rows whose outputs are not written).
-__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t, int pair = 0) {
+__device__ __forceinline__ TileCoord decode_tile(const GemmParams& p, int t) {
   const int rb = p.raster_bands;
   const int per_group = rb * p.n_wtiles;
   const int g = t / per_group;
   const int idx = t - g * per_group;
-  const int gm = min(rb, p.n_xunits - g * rb);
+  const int gm = min(rb, p.n_xtiles - g * rb);
   const int w = idx / gm;
   TileCoord c;
-  c.xt = (g * rb + (idx - w * gm)) * p.xgroup + pair;
+  c.xt = g * rb + (idx - w * gm);
   int j = 0;
 #pragma unroll 1
   while (j + 1 < p.n_lin && w >= p.wtile_start[j + 1]) ++j;
@@ -283,12 +277,7 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
 // division stays out of the common kernel's unrolled epilogue).
 // YTMA: Y leaves through shared memory and tensor-map stores (Y_ROWS rows x
 // 128 features per store) instead of per-thread global stores.
-// MC (with CG = 2): clusters of four CTAs, two pairs that work on the same
-// weight tile and two bands at once. Each CTA loads half of its 128 weight
-// rows and multicasts it to the CTA of the other pair that holds the same
-// rows, so each weight row is read from L2 once per cluster; a stage is
-// refilled once both pairs' MMAs have released it.
-template <int CG, int BN_, bool UNSCALE, bool YTMA, bool MC = false>
+template <int CG, int BN_, bool UNSCALE, bool YTMA>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   using Gm = Geom<CG, BN_, YTMA>;
@@ -311,25 +300,21 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   int* err = &g_device_error;
-  static_assert(!MC || CG == 2, "multicast clusters are made of CTA pairs");
-  constexpr int UNIT_CTAS = MC ? 4 : CG;  // CTAs per scheduling unit (cluster)
-  // CTA rank in the cluster and in its pair (0 issues the pair's MMAs), the
-  // pair within the cluster, and the scheduling unit (a cluster or a CTA)
+  constexpr int UNIT_CTAS = CG;  // CTAs per scheduling unit (a pair or a CTA)
+  // CTA rank in its pair (0 issues the pair's MMAs) and the scheduling unit
   const uint32_t crank = (CG == 2) ? cluster_ctarank() : 0u;
-  const uint32_t rank = crank & 1u;
-  const uint32_t pair = MC ? (crank >> 1) : 0u;
-  const uint32_t lead_rank = crank & ~1u;  // the pair leader's rank in the cluster
+  const uint32_t rank = crank;
+  const uint32_t lead_rank = 0u;  // the pair leader's rank in the cluster
   const bool leader = (rank == 0);
   const int unit = (CG == 2) ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
   const int n_units = (CG == 2) ? static_cast<int>(cluster_count_x()) : static_cast<int>(gridDim.x);
-  // CTAs whose stages a pair's MMAs release, and the pair's own CTAs
-  const uint16_t release_mask = MC ? 0xFu : 0x3u;
-  const uint16_t pair_mask = static_cast<uint16_t>(0x3u << lead_rank);
+  // the pair's CTAs: a pair's MMA commits arrive on both
+  const uint16_t pair_mask = 0x3u;
 
   if (threadIdx.x == PRODUCER_WARP * 32) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC ? 2 : 1);  // one release per pair that reads the stage
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -365,15 +350,12 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       const uint64_t pol_w = l2_policy_evict_normal();
       // the pair's "full" barriers live in the leader CTA
       const uint32_t full_leader = (CG == 2) ? mapa_shared(smem_u32(full), lead_rank) : smem_u32(full);
-      // MC: this CTA's half of its weight rows, multicast to itself and the
-      // CTA of the other pair with the same rank
-      const uint16_t w_mask = static_cast<uint16_t>((1u << rank) | (1u << (2 + rank)));
       uint32_t stage = 0, phase = 0;
       uint32_t n_issued = 0;  // stage loads issued so far (stage = n % STAGES)
       bool ok = true;
       WorkItem it;
       for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
-        const TileCoord c = decode_tile(p, it.t, static_cast<int>(pair));
+        const TileCoord c = decode_tile(p, it.t);
         const int w_row = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
         const int x_row = c.xt * BN + static_cast<int>(rank) * Gm::X_ROWS;
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
@@ -383,11 +365,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           if (CG == 2) {
             if (leader) mbar_arrive_expect_tx(&full[stage], CG * Gm::STAGE_BYTES);
             const uint32_t fb = full_leader + stage * 8u;
-            if (MC)
-              tma_load_2d_pair_mc(sw + pair * (Gm::W_BYTES / 2), &p.tmap_w[c.lin], fb, kb * BK,
-                                  w_row + static_cast<int>(pair) * (CTA_M / 2), w_mask, pol_w);
-            else
-              tma_load_2d_pair(sw, &p.tmap_w[c.lin], fb, kb * BK, w_row, pol_w);
+            tma_load_2d_pair(sw, &p.tmap_w[c.lin], fb, kb * BK, w_row, pol_w);
             tma_load_2d_pair(sx, &p.tmap_x, fb, kb * BK, x_row, pol_x);
           } else {
             mbar_arrive_expect_tx(&full[stage], Gm::STAGE_BYTES);
@@ -445,7 +423,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
               if (CG == 2) mma_f16_ss_pair(d_tmem, a_desc + koff, b_desc + koff, Gm::IDESC, acc);
               else mma_f16_ss(d_tmem, a_desc + koff, b_desc + koff, Gm::IDESC, acc);
             }
-            if (CG == 2) mma_commit_pair(&empty[stage], release_mask); else mma_commit(&empty[stage]);
+            if (CG == 2) mma_commit_pair(&empty[stage], pair_mask); else mma_commit(&empty[stage]);
             if (++stage == STAGES) { stage = 0; phase ^= 1u; }
           }
           if (!ok) break;
@@ -473,7 +451,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     bool ok = true;
     WorkItem it;
     for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
-      const TileCoord c = decode_tile(p, it.t, static_cast<int>(pair));
+      const TileCoord c = decode_tile(p, it.t);
       const int L = tile_chunk_kb<CG>(p, c);
       // One exact chunk (the whole K of a tile that is not split) is kept as
       // the fp32 value TMEM holds: an integer below 2^24, so it is float(A)
@@ -723,18 +701,16 @@ int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   return CONVROT_OK;
 }
 
-// xgroup: bands per unit of work (2 for clusters of two pairs, whose CTAs
-// load weight rows in boxes of 64).
 template <int CG, int BN>
 int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, int64_t K,
-                const GemmLinear* lins, int n_lin, bool raw_s32, int xgroup = 1) {
+                const GemmLinear* lins, int n_lin, bool raw_s32) {
   using Gm = Geom<CG, BN>;
   memset(&p, 0, sizeof(p));
   int st = make_tmap(&p.tmap_x, x16, M, K, Gm::X_ROWS);
   if (st) return st;
   int wt = 0;
   for (int j = 0; j < n_lin; ++j) {
-    st = make_tmap(&p.tmap_w[j], lins[j].w16, lins[j].N, K, xgroup == 2 ? CTA_M / 2 : CTA_M);
+    st = make_tmap(&p.tmap_w[j], lins[j].w16, lins[j].N, K, CTA_M);
     if (st) return st;
     p.s_w[j] = lins[j].s_w;
     p.bias[j] = lins[j].bias;
@@ -751,12 +727,10 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
   p.K = static_cast<int>(K);
   p.num_kb = static_cast<int>((K + BK - 1) / BK);
   p.n_xtiles = static_cast<int>((M + BN - 1) / BN);
-  p.xgroup = xgroup;
-  p.n_xunits = (p.n_xtiles + xgroup - 1) / xgroup;
   p.n_wtiles = wt;
-  const int64_t unit_bytes = static_cast<int64_t>(BN) * K * 2 * xgroup;
-  p.raster_bands = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.n_xunits, RASTER_L2_BYTES / unit_bytes)));
-  const int64_t total = static_cast<int64_t>(p.n_xunits) * wt;
+  const int64_t band_bytes = static_cast<int64_t>(BN) * K * 2;
+  p.raster_bands = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(p.n_xtiles, RASTER_L2_BYTES / band_bytes)));
+  const int64_t total = static_cast<int64_t>(p.n_xtiles) * wt;
   if (total > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
   p.total_tiles = static_cast<int>(total);
   p.n_lin = n_lin;
@@ -803,7 +777,7 @@ void plan_split(GemmParams& p, int units, int unit_ctas, const GemmSync& sync) {
 }
 
 // Raise the kernel's shared-memory limit once per device.
-template <int CG, int BN, bool UNSCALE, bool YTMA, bool MC = false>
+template <int CG, int BN, bool UNSCALE, bool YTMA>
 int configure_kernel() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -812,7 +786,7 @@ int configure_kernel() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE, YTMA, MC>,
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE, YTMA>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Geom<CG, BN, YTMA>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
@@ -820,12 +794,13 @@ int configure_kernel() {
   return CONVROT_OK;
 }
 
-// Launch configuration of the CTA-pair kernel: n_units clusters of
-// `cluster` CTAs (a pair, or two pairs) and, when `pdl`, programmatic
-// serialization after the previous kernel in the stream (the kernel waits for
-// it with griddepcontrol.wait after its own setup).
+// Launch configuration of the CTA-pair kernel: n_units clusters of two CTAs
+// and, when `pdl`, programmatic serialization after the previous kernel in
+// the stream (the kernel waits for it with griddepcontrol.wait after its own
+// setup).
 cudaLaunchConfig_t pair_config(int n_units, size_t smem, cudaStream_t stream, cudaLaunchAttribute* attr,
-                               bool pdl = false, int cluster = 2) {
+                               bool pdl = false) {
+  constexpr int cluster = 2;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = cluster;
   attr[0].val.clusterDim.y = 1;
@@ -842,10 +817,9 @@ cudaLaunchConfig_t pair_config(int n_units, size_t smem, cudaStream_t stream, cu
   return cfg;
 }
 
-// Co-resident clusters (CTA pairs, or with MC clusters of two pairs) of the
-// BN variant on the current device (0 if they cannot launch), cached per
-// device. The kernel must be configured first.
-template <int BN, bool MC = false>
+// Co-resident CTA pairs of the BN variant on the current device (0 if they
+// cannot launch), cached per device. The kernel must be configured first.
+template <int BN>
 int max_pairs() {
   static std::mutex mu;
   static int cached[64];
@@ -855,10 +829,9 @@ int max_pairs() {
   std::lock_guard<std::mutex> lock(mu);
   if (!known[dev]) {
     cudaLaunchAttribute attr[2];
-    cudaLaunchConfig_t cfg =
-        pair_config(device_sm_count() / (MC ? 4 : 2), Geom<2, BN, true>::SMEM_ALLOC, nullptr, attr, false, MC ? 4 : 2);
+    cudaLaunchConfig_t cfg = pair_config(device_sm_count() / 2, Geom<2, BN, true>::SMEM_ALLOC, nullptr, attr, false);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false, true, MC>, &cfg) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveClusters(&n, convrot_gemm_kernel<2, BN, false, true>, &cfg) != cudaSuccess) {
       cudaGetLastError();  // clear the sticky launch-query error
       n = 0;
     }
@@ -868,23 +841,22 @@ int max_pairs() {
   return cached[dev];
 }
 
-// `pairs`: co-resident clusters of the variant (pairs, or MC clusters of two pairs).
-template <int BN, bool UNSCALE, bool YTMA, bool MC = false>
+// `pairs`: co-resident CTA pairs of the variant.
+template <int BN, bool UNSCALE, bool YTMA>
 int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
                  bool raw_s32, int pairs, cudaStream_t stream, const GemmSync& sync) {
   GemmParams p;
-  if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, raw_s32, MC ? 2 : 1)) return st;
+  if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, raw_s32)) return st;
   if (p.total_tiles == 0) return CONVROT_OK;
   if (YTMA)
     for (int j = 0; j < n_lin; ++j)
       if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
   const int units = std::min(p.total_tiles, pairs);
-  if (BN == 256) plan_split(p, units, MC ? 4 : 2, sync);
+  if (BN == 256) plan_split(p, units, 2, sync);
   cudaLaunchAttribute attr[2];
-  const cudaLaunchConfig_t cfg =
-      pair_config(units, Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true, MC ? 4 : 2);
-  if (int st = configure_kernel<2, BN, UNSCALE, YTMA, MC>()) return st;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE, YTMA, MC>, p);
+  const cudaLaunchConfig_t cfg = pair_config(units, Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true);
+  if (int st = configure_kernel<2, BN, UNSCALE, YTMA>()) return st;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, UNSCALE, YTMA>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
   return check_launch();
 }
@@ -988,27 +960,6 @@ int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool
   return best;
 }
 
-// Clusters of two pairs (weight rows multicast between the pairs) instead of
-// single pairs, for 256-row tiles. Multicast reads a quarter fewer operand
-// bytes from L2, which measured as 5.5 % less time per tile and SM, but fewer
-// clusters of four fit the GPU than pairs (144 of 152 SMs on GB300) and a
-// unit of work is two bands. Modelled time in tile-times: waves of units,
-// fractional where the split balances them, times 0.945 for multicast; it is
-// chosen when that is at least 1 % below the pairs' time.
-bool use_multicast(int64_t M, const GemmLinear* lins, int n_lin, int pairs, int quads, bool can_split) {
-  if (quads <= 0 || pairs <= 0) return false;
-  int64_t wtiles = 0;
-  for (int j = 0; j < n_lin; ++j) wtiles += (lins[j].N + 2 * CTA_M - 1) / (2 * CTA_M);
-  const int64_t bands = (M + 255) / 256;
-  const int64_t t_pairs = bands * wtiles, t_quads = (bands + 1) / 2 * wtiles;
-  if (t_pairs > 0x7fffffff) return false;
-  auto waves = [&](int64_t T, int units) {
-    const bool split = can_split && split_pays(static_cast<int>(T), units);
-    return split ? static_cast<double>(T) / units : static_cast<double>((T + units - 1) / units);
-  };
-  return 0.945 * waves(t_quads, quads) < 0.99 * waves(t_pairs, pairs);
-}
-
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream, GemmSync sync) {
   if (M == 0) return CONVROT_OK;
@@ -1024,16 +975,6 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
   if (pairs > 0) {
     const bool can_split = sync.words && sync.bytes >= static_cast<size_t>(2 * pairs) * sizeof(unsigned long long);
     const int bn = pick_tile_rows(M, lins, n_lin, pairs, can_split);
-    if (bn == 256 && !unscale) {
-      if (int st = configure_kernel<2, 256, false, true, true>()) return st;
-      if (int st = configure_kernel<2, 256, false, false, true>()) return st;
-      const int quads = std::min(max_pairs<256, true>(), max_pairs<256, false>() / 2);
-      const bool can_split4 = sync.words && sync.bytes >= static_cast<size_t>(4 * quads) * sizeof(unsigned long long);
-      if (use_multicast(M, lins, n_lin, pairs, quads, can_split && can_split4)) {
-        if (ytma) return launch_pairs<256, false, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, quads, stream, sync);
-        return launch_pairs<256, false, false, true>(x16, s_x, M, K, lins, n_lin, raw_s32, quads, stream, sync);
-      }
-    }
     if (ytma && unscale) {
       if (bn == 128) return launch_pairs<128, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
       if (bn == 192) return launch_pairs<192, true, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);

@@ -15,7 +15,12 @@
 // In host code its name is a host-side stand-in, not a device address, so its
 // device address is looked up with cudaGetSymbolAddress, with that device
 // current, by the first call on each device, and then passed to the kernels.
-// That first call on a device should therefore come before any stream capture.
+// The address is remembered together with the identity of the CUDA context
+// it was looked up in; a call made in another context (for instance after
+// cudaDeviceReset replaced the device's primary context) looks it up again,
+// so no call ever uses an address of a context that no longer exists. The
+// first call on a device (or in a new context) should therefore come before
+// any stream capture.
 // All calls on a device share the array and it keeps the last call's
 // contents; nothing in it needs to start at zero, because the pack writes
 // every code and scale that the GEMM then reads. Calls that overlap on the
@@ -36,24 +41,56 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // the context the address belongs to (0: none yet)
+  void* addr = nullptr;
+};
+ScratchAddr g_scratch_addr[kMaxDevices];  // per device
 
-// Device address of the array on the current device, looked up on the first
-// call for that device.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the calling thread's current CUDA context (0 if there is none).
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the array in the current device's current context,
+// looked up on the first call in that context.
 int scratch_address(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return set_cuda_error(e);
   if (dev < 0 || dev >= kMaxDevices) return CONVROT_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  const unsigned long long ctx = current_context_id();
+  if (ctx == 0 || ctx != a.ctx_id || !a.addr) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);  // makes the device's context current if needed
     if (e != cudaSuccess) return set_cuda_error(e);
     if (!p) return set_cuda_error(cudaErrorInvalidSymbol);
-    g_scratch_addr[dev] = p;
+    a.addr = p;
+    a.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = a.addr;
   return CONVROT_OK;
 }
 

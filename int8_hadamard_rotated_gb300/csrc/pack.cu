@@ -24,9 +24,14 @@
 // 1.5 * 2^23 magic constant (round-half-even). |q - RN(z/d)| < 1.9e-5 for
 // |z/d| <= 127.0001, so whenever q is farther than 2^-15 from a half-integer
 // both round to the same integer; the rare values nearer than that are
-// recomputed with the IEEE division. |z/d| <= 127 (1 + 2^-23) because d is
-// max|z| / 127 rounded once, so the rounded code already lies in [-127, 127]
-// and the clamp of the definition never changes it.
+// recomputed as rint(RN(RN(z 2^-n) / s)), the definition's two roundings
+// (RN(z 2^-n) is X_rot itself, exact unless X_rot is subnormal). When s is a
+// normal float, |z/d| <= 127 (1 + 2^-23) because d is max|z| / 127 rounded
+// once, so the rounded code already lies in [-127, 127] and the clamp of the
+// definition never changes it. A row whose s is subnormal (max |X_rot| below
+// about 127 * 2^-126) has lost precision in s, so codes beyond 127 can occur
+// and 1/d can overflow: every code of such a row takes the definition's
+// division and clamp.
 //
 // Data layout. A thread owns 64 elements of one row: four "units" of 16
 // consecutive elements (index bits 0-3 in registers). For G >= 64 the four
@@ -161,6 +166,7 @@ constexpr int kMaxThreads = 512;
 constexpr int kMaxRowsPerCta = 256;
 constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
 constexpr float kNearHalf = 0.5f - 1.0f / 32768.0f;  // 0.5 - 2^-15
+constexpr float kMinNormal = 1.17549435082228751e-38f;  // 2^-126, the smallest normal float
 
 // Parameters of the modulation prologue (kProModulate).
 struct ModPrologue {
@@ -327,10 +333,25 @@ __device__ __forceinline__ float held_divisor(float s, int flip) {
   return flip ? -d : d;
 }
 
+// The code of held value z by the definition: rint(X_rot / s) with
+// X_rot = RN(z 2^-n) and s = d 2^-n (exact: a power-of-two scaling of the
+// divisor, sign included), clamped to [-127, 127].
+template <int G>
+__device__ __forceinline__ float exact_code(float z, float d) {
+  const float q = rintf(__fdiv_rn(__fmul_rn(z, Geo<G>::kInvScale), __fmul_rn(d, Geo<G>::kInvScale)));
+  return fminf(fmaxf(q, -127.0f), 127.0f);
+}
+
 // Codes of unit j (rounded quotients as integer-valued floats), in output order.
+// tiny_row: s is subnormal, so every code takes the definition's division.
 template <int G>
 __device__ __forceinline__ void quantize_unit(const float (&vj)[16], int j, float d, float rcp, bool zero_row,
-                                              float (&qr)[16]) {
+                                              bool tiny_row, float (&qr)[16]) {
+  if (tiny_row) {
+#pragma unroll
+    for (int p = 0; p < 16; ++p) qr[out_pos<G>(p)] = exact_code<G>(static_sign<G>(j, p) ? -vj[p] : vj[p], d);
+    return;
+  }
   const unsigned long long rcp2 = f2pack(rcp, rcp);
   const unsigned long long magic2 = f2pack(kMagic, kMagic);
   bool near_half = false;
@@ -356,7 +377,7 @@ __device__ __forceinline__ void quantize_unit(const float (&vj)[16], int j, floa
       const float z = static_sign<G>(j, p) ? -vj[p] : vj[p];
       const float q = z * rcp;
       const float tt = (q + kMagic) - kMagic;
-      if (fabsf(q - tt) > kNearHalf) qr[out_pos<G>(p)] = rintf(__fdiv_rn(z, d));
+      if (fabsf(q - tt) > kNearHalf) qr[out_pos<G>(p)] = exact_code<G>(z, d);
     }
   }
   if (zero_row) {
@@ -630,7 +651,8 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
     if (t == 0) scales[row] = s;
     const float d = held_divisor<G>(s, ls.flip);
     const bool zero_row = (s == 0.0f);
-    const float rcp = zero_row ? 0.0f : __frcp_rn(d);
+    const bool tiny_row = !zero_row && s < kMinNormal;
+    const float rcp = (zero_row || tiny_row) ? 0.0f : __frcp_rn(d);
 
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -638,7 +660,7 @@ pack_kernel(const TIn* __restrict__ X, int64_t M, int K, int tpr, int rpc, int64
       if (u >= units) continue;
       const int uo = out_unit<G>(u, gi, li, j);
       float qr[16];
-      quantize_unit<G>(v[j], j, d, rcp, zero_row, qr);
+      quantize_unit<G>(v[j], j, d, rcp, zero_row, tiny_row, qr);
       if (OUT == kPackI8) {
         int8_t* dst = static_cast<int8_t*>(out_codes) + row * static_cast<int64_t>(K) + 16 * uo;
         *reinterpret_cast<uint4*>(dst) = codes_i8(qr);
@@ -847,14 +869,15 @@ pack_tma_kernel(const __grid_constant__ PackTmaParams p) {
       if (t == 0) p.scales[row] = s;
       const float d = held_divisor<G>(s, ls.flip);
       const bool zero_row = (s == 0.0f);
-      const float rcp = zero_row ? 0.0f : __frcp_rn(d);
+      const bool tiny_row = !zero_row && s < kMinNormal;
+      const float rcp = (zero_row || tiny_row) ? 0.0f : __frcp_rn(d);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int u = u_of[j];
         if (u >= units) continue;
         const int uo = out_unit<G>(u, gi, li, j);
         float qr[16];
-        quantize_unit<G>(v[j], j, d, rcp, zero_row, qr);
+        quantize_unit<G>(v[j], j, d, rcp, zero_row, tiny_row, qr);
         uint8_t* dst = sbuf + static_cast<size_t>(lr * K + 16 * uo) * OSZ;
         if (OUT == kPackI8) {
           *reinterpret_cast<uint4*>(dst) = codes_i8(qr);

@@ -97,7 +97,6 @@ SIGNATURES = {
                          ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_device_status": (_I, [_VP]),
-    "convrot_probe_int8_mma_rate": (_I, [_I, ctypes.POINTER(ctypes.c_double)]),
 }
 
 
@@ -474,10 +473,3 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
 
 def convrot_device_status(stream=None) -> int:
     return int(lib().convrot_device_status(_stream(stream)))
-
-
-def convrot_probe_int8_mma_rate(iters: int = 20000) -> float:
-    """Diagnostic: the legacy mma.sync s8 tensor rate of the current device, in TOPS."""
-    out = ctypes.c_double(0.0)
-    _check(lib().convrot_probe_int8_mma_rate(int(iters), ctypes.byref(out)), "convrot_probe_int8_mma_rate")
-    return float(out.value)

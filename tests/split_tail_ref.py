@@ -55,18 +55,3 @@ def tile_rows(M: int, Ns, pairs: int, can_split: bool) -> int:
         if best_cost is None or cost < best_cost:
             best, best_cost = bn, cost
     return best
-
-
-def use_multicast(M: int, Ns, pairs: int, quads: int, can_split: bool) -> bool:
-    """Whether the launcher takes clusters of two pairs for 256-row tiles."""
-    if quads <= 0:
-        return False
-    wtiles = sum((n + 255) // 256 for n in Ns)
-    bands = -(-M // 256)
-    t_pairs, t_quads = bands * wtiles, (bands + 1) // 2 * wtiles
-
-    def waves(T, units):
-        if can_split and split_pays(T, units):
-            return T / units
-        return -(-T // units)
-    return 0.945 * waves(t_quads, quads) < 0.99 * waves(t_pairs, pairs)

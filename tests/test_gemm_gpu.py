@@ -131,9 +131,19 @@ def test_empty_shapes(ops):
     assert A.shape == (4, 0)
 
 
-def test_int8_mma_rate_probe_runs(ops):
-    """The diagnostic microbenchmark of the legacy s8 tensor instruction runs
-    and reports a positive, finite rate."""
+def test_bench_probes_run(ops):
+    """The benchmark's own kernels (libconvrot_bench.so): the probe of the
+    legacy s8 tensor instruction reports a positive, finite rate, and the
+    size-matched copy writes every output byte."""
     import math
-    tops = ops.convrot_probe_int8_mma_rate(2000)
+    import bench
+    tops = bench.int8_mma_rate(2000)
     assert math.isfinite(tops) and tops > 0.0
+    X = torch.arange(12 * 64, dtype=torch.float32, device="cuda").reshape(12, 64) % 100
+    out = torch.full((12, 64), 0xEE, dtype=torch.uint8, device="cuda")
+    sc = torch.full((12,), 1.0, dtype=torch.float32, device="cuda")
+    st = bench.bench_lib().bench_copy_ceiling(X.data_ptr(), 12, 64, 1, out.data_ptr(), sc.data_ptr(), 1,
+                                              torch.cuda.current_stream().cuda_stream)
+    assert st == 0
+    np.testing.assert_array_equal(host(out), host(X).astype(np.int64).astype(np.uint8))
+    assert not host(sc).any()

@@ -527,6 +527,59 @@ def test_linear_scaled_pins():
     assert np.max(np.abs(wrong - Y)) > 0.5 * np.max(np.abs(Y))
 
 
+def check_prologue(mod=orc):
+    """The modulation prologue on hand-computed values where every step of
+    its definition shows: the RMS norm divides by sqrt(mean(x^2) + eps), with
+    eps under the square root and the mean over the row's length; then the
+    weight; then (x + x * scale) + shift."""
+    f32 = np.float32
+    # rows of +-1 (mean x^2 = 1) with eps = 3: 1 / sqrt(1 + 3) = 0.5 exactly,
+    # where eps outside the root, 1 / (sqrt(1) + 3), would give 0.25
+    x = np.array([[1.0, -1.0, 1.0, 1.0], [-1.0, -1.0, 1.0, -1.0]], f32)
+    np.testing.assert_array_equal(mod.prologue(x, rmsnorm=True, eps=3.0), x * f32(0.5))
+    # the mean, not the sum: a row of +-2 of length 4 has mean x^2 = 4;
+    # eps = 12 gives 1 / sqrt(16) = 0.25, so x * r = +-0.5
+    y = np.array([[2.0, -2.0, 2.0, 2.0]], f32)
+    np.testing.assert_array_equal(mod.prologue(y, rmsnorm=True, eps=12.0), y * f32(0.25))
+    # the order of the per-channel steps: ((x * r) * w + (x * r) * w * scale) + shift
+    z = np.array([[1.0, -1.0, 1.0, -1.0]], f32)
+    got = mod.prologue(z, rmsnorm=True, eps=3.0, weight=np.full(4, 4.0, f32), scale=np.full(4, 0.5, f32),
+                       shift=np.full(4, 1.0, f32))
+    # x r = +-0.5; times 4 = +-2; (+-2 + +-2 * 0.5) = +-3; + 1 = 4 or -2
+    np.testing.assert_array_equal(got, np.array([[4.0, -2.0, 4.0, -2.0]], f32))
+
+
+def test_prologue_eps_and_order():
+    check_prologue()
+
+
+def _prologue_eps_outside_root(X, rmsnorm=False, eps=1e-6, weight=None, scale=None, shift=None):
+    x = np.asarray(X).astype(np.float32)
+    if rmsnorm:
+        ms = (x.astype(np.float64) ** 2).mean(axis=1)
+        x = (x / (np.sqrt(ms) + eps)[:, None]).astype(np.float32)
+    return orc.prologue(x, False, eps, weight, scale, shift)
+
+
+def _prologue_sum_not_mean(X, rmsnorm=False, eps=1e-6, weight=None, scale=None, shift=None):
+    x = np.asarray(X).astype(np.float32)
+    if rmsnorm:
+        ss = (x.astype(np.float64) ** 2).sum(axis=1)
+        x = (x / np.sqrt(ss + eps)[:, None]).astype(np.float32)
+    return orc.prologue(x, False, eps, weight, scale, shift)
+
+
+def _prologue_shift_then_scale(X, rmsnorm=False, eps=1e-6, weight=None, scale=None, shift=None):
+    x = orc.prologue(X, rmsnorm, eps, weight, None, shift)
+    return orc.prologue(x, False, eps, None, scale, None)
+
+
+@pytest.mark.parametrize("bad", [_prologue_eps_outside_root, _prologue_sum_not_mean, _prologue_shift_then_scale],
+                         ids=["eps-outside-root", "sum-not-mean", "shift-before-scale"])
+def test_planted_prologue_mistakes_are_caught(bad):
+    assert _fails(_Mutant(prologue=bad), (check_prologue,))
+
+
 def test_prologue_pins():
     """The modulation prologue against values fixed by its definition."""
     import numpy as np

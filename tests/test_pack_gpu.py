@@ -182,3 +182,54 @@ def test_binary16_code_output(ops, M, K, G, dtype):
     assert_scales(s, so)
     assert np.array_equal(Q16, np.rint(Q16)) and np.abs(Q16).max() <= 127
     assert_codes(Q16.astype(np.int32), Qo)
+
+
+@pytest.mark.parametrize("G", [1, 4, 16, 64, 256, 1024])
+def test_rows_with_subnormal_scales(ops, G):
+    """Rows whose rotated maximum lies below about 127 * 2^-126, so that
+    s = max|X_rot| / 127 is a subnormal float with few significant bits:
+    quotients can then exceed 127 and must clamp, and 1 / (s 2^n) can
+    overflow. The values are small integers times a power of two, so every
+    sum of the rotation is exact in fp32 and the GPU must match the oracle
+    exactly; the smallest rows round to s = 0 (a zero row)."""
+    K = 2048
+    rng = workloads.rng_for(7100 + G)
+    rows = []
+    for e in (-120, -126, -128, -133, -138, -141, -145, -149):
+        k = rng.integers(-50, 51, size=K).astype(np.float64)
+        k[rng.integers(0, K)] = 50.0
+        rows.append(k * 2.0 ** e)
+    # +-1 and 0 times 2^-149: max |X_rot| <= 2^(n-149) <= 32 * 2^-149, so s rounds to 0
+    rows.append(rng.integers(-1, 2, size=K).astype(np.float64) * 2.0 ** -149)
+    X = np.array(rows).astype(np.float32)
+    assert np.array_equal(X.astype(np.float64), np.array(rows))   # exactly representable
+    for dtype_out in ("i8", "f16"):
+        if dtype_out == "i8":
+            Q, s = gpu_pack(ops, X, G)
+        else:
+            Q16, s16 = ops.convrot_pack_activations_f16(dev(X), G)
+            Q, s = host(Q16).astype(np.int32), host(s16)
+        Qo, so = oracle.pack(X, G)
+        np.testing.assert_array_equal(s, so)
+        np.testing.assert_array_equal(np.asarray(Q, np.int32), Qo.astype(np.int32))
+        assert np.any((so > 0) & (so < np.float32(2.0 ** -126)))        # some scales are subnormal
+        assert np.any(so == 0)                                          # and the smallest rows are zero rows
+
+
+def test_rows_of_tiny_random_values(ops):
+    """Random rows of magnitudes 1e-37 down to 1e-44 (subnormal inputs
+    included): codes stay in [-127, 127]; where the GPU's scale equals the
+    oracle's (the rotation sums round differently in fp32, which can move a
+    subnormal scale by one unit), the codes agree within the usual bar."""
+    K, G = 3072, 256
+    rng = workloads.rng_for(7200)
+    mags = np.repeat([1e-37, 1e-38, 1e-39, 1e-40, 1e-41, 1e-42, 1e-43, 1e-44], 4)
+    X = (rng.standard_normal((len(mags), K)) * mags[:, None]).astype(np.float32)
+    Q, s = gpu_pack(ops, X, G)
+    Qo, so = oracle.pack(X, G)
+    assert np.isfinite(s).all() and np.abs(Q.astype(np.int32)).max() <= 127
+    same = s == so
+    assert same.sum() >= 0.75 * len(s)
+    assert_codes(Q[same], Qo[same])
+    ulp = np.float32(2.0 ** -149)
+    assert np.all(np.abs(s.astype(np.float64) - so) <= np.maximum(1e-6 * so, ulp))

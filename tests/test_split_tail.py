@@ -8,7 +8,7 @@ import itertools
 
 import pytest
 
-from split_tail_ref import plan_split, work_items, tile_rows, use_multicast
+from split_tail_ref import plan_split, work_items, tile_rows
 
 
 @pytest.mark.parametrize("T,units,num_kb", list(itertools.product(
@@ -74,13 +74,3 @@ def test_tile_height_choice():
     assert tile_rows(4096, [1280], 76, True) == 192   # only 256-row tiles split
     # one wave either way: the shortest tile gives the most parallelism
     assert tile_rows(256, [3072], 76, True) == 128
-
-
-def test_multicast_choice():
-    # 76 pairs, 36 clusters of two pairs (GB300)
-    assert not use_multicast(4608, [3072] * 3, 76, 36, True)   # 8.53 split waves vs 9 x 0.945
-    assert use_multicast(4608, [3072], 76, 36, True)           # MLP down: 3 vs 3 x 0.945
-    assert not use_multicast(4864, [3072] * 3, 76, 36, True)   # 10 x 0.945 vs 9
-    assert use_multicast(1024, [9472], 76, 36, True)           # 2 waves vs 74 units split over 36
-    assert use_multicast(2597, [2148], 76, 36, True)           # 11 bands: an odd band count
-    assert not use_multicast(4608, [3072], 76, 0, True)        # no clusters of four

@@ -1,8 +1,7 @@
 """GPU checks of the GEMM's work distribution: split waves (the K-split whose
 partial int32 sums pass between CTA pairs through the tile's output and a
-hand-over word) and clusters of two pairs that multicast weight rows. The
-int32 product stays bit-exact against the oracle on ragged shapes that take
-these paths (odd band counts included), results are identical with and
+hand-over word). The int32 product stays bit-exact against the oracle on
+ragged shapes that take this path (odd band counts included), results are identical with and
 without the split, the hand-over words are left zero after use, and a
 CUDA-graph replay (the same launch, hence the same hand-over value, again and
 again) stays correct."""
@@ -28,8 +27,8 @@ def codes(seed, rows, cols, amp=127):
     (2597, 2148, 4160, False),   # the same with the fixed 1024-product chunks
     (768, 9216, 3072, True),     # a host-pipeline chunk of the DiT projections: 108 tiles
     (300, 20000, 1040, False),   # 2 x 79 tiles, K not a multiple of 1024
-    (1024, 9472, 3072, True),    # clusters of two pairs with a split: 74 units of two tiles
-    (4608, 3072, 12288, True),   # clusters of two pairs, K = 12288 in runs of >= 4096
+    (1024, 9472, 3072, True),    # 148 tiles: under two waves, whole tiles
+    (4608, 3072, 12288, True),   # 216 tiles, K = 12288 in runs of >= 4096
 ])
 def test_exact_int32_with_split_tiles(ops, M, N, K, use_plan):
     Qx = codes(M + K, M, K)
