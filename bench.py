@@ -639,8 +639,8 @@ def next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step,
     launching stream, mean over `reps`): the pack with the modulation prologue
     (RMS norm, per-channel weight, (x + x*scale) + shift) beside the plain
     pack of the same X; the one-call linear with an input scale beside the
-    plain one-call linear; the expansion of packed 4-bit weights of one
-    projection. Not part of the step."""
+    plain one-call linear; the three projections as W4A4 linears (packed
+    signed 4-bit weights read by the S8 x S4 GEMM). Not part of the step."""
     import torch
     from int8_hadamard_rotated_gb300 import ops
 
@@ -690,22 +690,38 @@ def next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step,
           "plain_linear_us": round(t_lin, 2), "plain_linear_TOPS": round(ops_step / (t_lin * 1e-6) / 1e12, 2)}
     del Ys, ws
 
-    # f3: packed signed 4-bit weights of one projection -> int8 and binary16 codes (offline)
-    N = q16s[0].shape[0]
-    P = torch.from_numpy(workloads.packed_int4(workloads.rng_for(12), N, K)).to(dev)
-    q8 = torch.empty((N, K), dtype=torch.int8, device=dev)
-    q16 = torch.empty((N, K), dtype=torch.float16, device=dev)
+    # f3: W4A4 linears -- the three projections with packed signed 4-bit
+    # weights (0.5 B per weight, read as they are by the S8 x S4 GEMM)
+    rng4 = workloads.rng_for(12)
+    P4 = [torch.from_numpy(workloads.packed_int4(rng4, q.shape[0], K)).to(dev) for q in q16s]
+    s4 = [torch.from_numpy((0.001 + 0.01 * rng4.random(q.shape[0])).astype(np.float32)).to(dev) for q in q16s]
+    Y4 = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=dev) for q in q16s]
+    w4desc = ops.make_weights(P4, s4, biases, Y4)
+    Q16 = torch.empty((M, K), dtype=torch.float16, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    sync_ws = torch.zeros((ops.GEMM_SYNC_BYTES,), dtype=torch.uint8, device=dev)
+    ops.convrot_pack_activations_f16(X, w.G, Q_x16=Q16, s_x=sx, stream=stream)
 
-    def expand():
-        st = L.convrot_w4_expand(P.data_ptr(), N, K, q8.data_ptr(), q16.data_ptr(), sp)
+    def gemm_w4():
+        st = L.convrot_linear_packed(Q16.data_ptr(), sx.data_ptr(), M, K, w4desc, len(P4), sync_ws.data_ptr(),
+                                     ops.GEMM_SYNC_BYTES, sp)
         if st:
-            raise ops.ConvrotError(st, "convrot_w4_expand")
-    t_w4 = timed(expand)
-    w4_bytes = N * K // 2 + N * K + N * K * 2
-    f3 = {"workload": f"packed 4-bit W [{N},{K}] -> int8 + binary16 codes (offline; the GEMM is the step's)",
-          "bound": "hbm", "bytes": w4_bytes, "us": round(t_w4, 2),
-          "GB/s": round(w4_bytes / (t_w4 * 1e-6) / 1e9, 1), "frac": round(w4_bytes / (t_w4 * 1e-6) / 1e9 / hbm, 4)}
-    return {"f2_pack_prologue": f2, "f4_input_scale": f4, "f3_w4_expand": f3,
+            raise ops.ConvrotError(st, "convrot_linear_packed (W4A4)")
+    t_g4 = timed(gemm_w4)
+    ws4 = torch.empty((ops.convrot_linear_workspace_size(M, K),), dtype=torch.uint8, device=dev)
+    t_l4 = timed(lambda: ops.convrot_linear(X, w.G, P4, s4, biases, Ys=Y4, workspace=ws4, stream=stream,
+                                            weights=w4desc))
+    n_w = sum(q.shape[0] for q in q16s)
+    f3 = {"workload": f"{w.name}: three W4A4 projections [{q16s[0].shape[0]},{K}] (packed signed 4-bit weights, "
+                      "F32 row scales) sharing one pack",
+          "bound": "tensor", "gemm_us": round(t_g4, 2), "gemm_TOPS": round(ops_step / (t_g4 * 1e-6) / 1e12, 2),
+          "linear_us": round(t_l4, 2), "linear_TOPS": round(ops_step / (t_l4 * 1e-6) / 1e12, 2),
+          "weight_bytes_read_per_launch": int(n_w * K // 2),
+          "weight_bytes_binary16_gemm": int(n_w * K * 2),
+          "note": "the S8 x S4 GEMM reads the packed bytes (TMA) and widens them to exact binary16 "
+                  "codes in shared memory; no expanded copy of the weights exists"}
+    del P4, Y4, ws4, Q16
+    return {"f2_pack_prologue": f2, "f4_input_scale": f4, "f3_w4a4_linear": f3,
             "note": "isolated launches, L2 flushed before each (launch latency included); "
                     "frac against the measured HBM copy peak"}
 

@@ -168,15 +168,31 @@ int int8_linear(const int8_t* Q_x, const float* s_x, int64_t M, int64_t K,
                 const float* bias, int64_t N, float* Y,
                 void* workspace, size_t workspace_bytes, void* stream);
 
-/* One linear of a convrot_linear call. */
+/* Longest K of a linear with packed 4-bit weights: 127 * 8 * 16384 < 2^24, so
+ * the whole product stays exact in the tensor cores' fp32 accumulator. */
+#define CONVROT_W4_MAX_K 16384
+
+/*
+ * One linear of a convrot_linear call. Its weight is either binary16 codes
+ * (q16, from convrot_prepare_weight) or, for the packed INT4 convrot format
+ * ("INT8 Convrot Safetensors", section "Packed INT4 convrot": convrot_w4a4,
+ * signed 4-bit weights, low nibble first, with an F32 per-output weight
+ * scale), the checkpoint's packed bytes (q4), which the S8 x S4 GEMM reads
+ * as they are: no expanded copy is made. Exactly one of q16 and q4 is set.
+ * A q4 linear needs K % 64 == 0 (ERR_ALIGN otherwise), K <= CONVROT_W4_MAX_K
+ * (ERR_UNSUPPORTED) and N % 4 == 0 (ERR_ALIGN); linears of both kinds may
+ * share one call (one GEMM launch per kind).
+ */
 typedef struct convrot_weight {
-  const uint16_t* q16; /* [N,K] binary16 weight codes (convrot_prepare_weight) */
+  const uint16_t* q16; /* [N,K] binary16 weight codes (convrot_prepare_weight), or NULL */
   const float* scale;  /* [N] s_w, or NULL (taken as 1) */
   const float* bias;   /* [N], or NULL (no bias) */
   int64_t N;           /* output features */
   float* Y;            /* [M,N] fp32 output */
   const int32_t* kchunk; /* [ceil(N/128)] exact-chunk plan from convrot_weight_chunks,
-                            or NULL (chunks of 1024 products) */
+                            or NULL (chunks of 1024 products); unused for q4 */
+  const uint8_t* q4;   /* [N,K/2] packed signed 4-bit weights (element 2j of a row
+                          in the low nibble of byte j), or NULL */
 } convrot_weight;
 
 /*
@@ -261,6 +277,23 @@ int int8_gemm_s32(const int8_t* Q_x, int64_t M, int64_t K,
                   const int8_t* Q_w, const uint16_t* Q_w16, const int32_t* kchunk,
                   int64_t N, int32_t* A, void* workspace, size_t workspace_bytes,
                   void* stream);
+
+/* Device bytes int8_gemm_s32_w4 needs: the widened Q_x and the GEMM's
+ * hand-over words (CONVROT_GEMM_SYNC_BYTES). */
+size_t int8_gemm_s32_w4_workspace_size(int64_t M, int64_t K);
+
+/*
+ * int8_gemm_s32_w4 -- the raw int32 product A = Q_x Q_w^T of int8 activation
+ * codes and packed signed 4-bit weights ("Packed INT4 convrot", low nibble
+ * first), through the S8 x S4 GEMM that the q4 linears of convrot_linear use.
+ * For exactness checks.
+ *   Q_x    [M,K] int8.   Q_w4 [N,K/2] packed bytes.   A [M,N] int32 (output).
+ *   K % 64 == 0 and K <= CONVROT_W4_MAX_K.
+ *   workspace  at least int8_gemm_s32_w4_workspace_size(M, K) bytes.
+ * Errors: ERR_ARG, ERR_ALIGN, ERR_UNSUPPORTED, ERR_ALIAS, ERR_WORKSPACE, ERR_CUDA.
+ */
+int int8_gemm_s32_w4(const int8_t* Q_x, int64_t M, int64_t K, const uint8_t* Q_w4, int64_t N,
+                     int32_t* A, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * convrot_pack_activations_f16 -- the pack of convrot_pack_activations, with

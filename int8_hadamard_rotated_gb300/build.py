@@ -27,7 +27,7 @@ LIB_DIR = os.path.join(PKG, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libconvrot.so")
 BENCH_LIB_PATH = os.path.join(LIB_DIR, "libconvrot_bench.so")
 
-SOURCES = ["api.cu", "pack.cu", "gemm.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu"]
+SOURCES = ["api.cu", "pack.cu", "gemm.cu", "gemm_w4.cu", "noalloc.cu", "host_pipeline.cu", "mlp.cu"]
 BENCH_CSRC = os.path.join(PKG, "bench_csrc")
 BENCH_SOURCES = ["copy_ceiling.cu", "mma_s8_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

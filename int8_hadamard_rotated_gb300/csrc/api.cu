@@ -56,6 +56,7 @@ bool device_is_sm103() {
 }
 
 int read_and_clear_device_error(cudaStream_t stream);  // gemm.cu: syncs, then the GEMM's word
+int read_and_clear_w4_error();                         // gemm_w4.cu: the S8 x S4 GEMM's word
 int read_and_clear_pack_error();                       // pack.cu: the pack kernels' word
 
 }  // namespace convrot
@@ -227,22 +228,29 @@ int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    if (!aligned16(w.q16) || !aligned16(w.Y) || (w.scale && !aligned16(w.scale)) || (w.bias && !aligned16(w.bias)) ||
-        (reinterpret_cast<uintptr_t>(w.kchunk) & 3u))
+    if (!aligned16(weight_codes(w)) || !aligned16(w.Y) || (w.scale && !aligned16(w.scale)) ||
+        (w.bias && !aligned16(w.bias)) || (reinterpret_cast<uintptr_t>(w.kchunk) & 3u))
       return CONVROT_ERR_ALIGN;
+    if (w.q4) {
+      // the S8 x S4 GEMM: 64-value blocks of K, whole 16-byte rows of Y, one exact fp32 run
+      if (K % 64 != 0 || w.N % 4 != 0) return CONVROT_ERR_ALIGN;
+      if (K > CONVROT_W4_MAX_K) return CONVROT_ERR_UNSUPPORTED;
+    }
   }
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
     if (w.N > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
-    const size_t ny = static_cast<size_t>(M) * w.N * 4, nk = static_cast<size_t>(w.N) * K * 2;
+    const size_t ny = static_cast<size_t>(M) * w.N * 4, nk = weight_code_bytes(w, K);
+    const void* wk = weight_codes(w);
     if (overlaps(w.Y, ny, in0, n0) || overlaps(w.Y, ny, in1, n1)) return CONVROT_ERR_ALIAS;
-    if (overlaps(in0, n0, w.q16, nk) || overlaps(in1, n1, w.q16, nk)) return CONVROT_ERR_ALIAS;
+    if (overlaps(in0, n0, wk, nk) || overlaps(in1, n1, wk, nk)) return CONVROT_ERR_ALIAS;
     for (int i = 0; i < n_weights; ++i) {
       const convrot_weight& v = weights[i];
       if (v.N == 0) continue;
-      const size_t vk = static_cast<size_t>(v.N) * K * 2;
-      if (overlaps(w.Y, ny, v.q16, vk) || overlaps(w.Y, ny, v.scale, v.N * 4) || overlaps(w.Y, ny, v.bias, v.N * 4))
+      const size_t vk = weight_code_bytes(v, K);
+      if (overlaps(w.Y, ny, weight_codes(v), vk) || overlaps(w.Y, ny, v.scale, v.N * 4) ||
+          overlaps(w.Y, ny, v.bias, v.N * 4))
         return CONVROT_ERR_ALIAS;
       if (i != j && overlaps(w.Y, ny, v.Y, static_cast<size_t>(M) * v.N * 4)) return CONVROT_ERR_ALIAS;
     }
@@ -253,9 +261,25 @@ int check_weights(const convrot_weight* weights, int n_weights, int64_t M, int64
 int check_weight_list(const convrot_weight* weights, int n_weights) {
   if (!weights || n_weights < 1 || n_weights > CONVROT_MAX_LINEARS) return CONVROT_ERR_ARG;
   for (int j = 0; j < n_weights; ++j) {
-    if (weights[j].N < 0) return CONVROT_ERR_ARG;
-    if (weights[j].N > 0 && (!weights[j].q16 || !weights[j].Y)) return CONVROT_ERR_ARG;
+    const convrot_weight& w = weights[j];
+    if (w.N < 0) return CONVROT_ERR_ARG;
+    if (w.N > 0 && (!w.Y || (!w.q16) == (!w.q4))) return CONVROT_ERR_ARG;  // exactly one kind of weight
   }
+  return CONVROT_OK;
+}
+
+int launch_linears(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
+                   bool raw_s32, cudaStream_t s, GemmSync sync) {
+  GemmLinear w16[CONVROT_MAX_LINEARS], w4[CONVROT_MAX_LINEARS];
+  int n16 = 0, n4 = 0;
+  for (int j = 0; j < n_lin; ++j) {
+    if (lins[j].N == 0) continue;
+    if (lins[j].w16) w16[n16++] = lins[j];
+    else w4[n4++] = lins[j];
+  }
+  if (n16 > 0)
+    if (int st = launch_gemm(x16, s_x, M, K, w16, n16, raw_s32, s, sync)) return st;
+  if (n4 > 0) return launch_gemm_w4(x16, s_x, M, K, w4, n4, raw_s32, s, sync);
   return CONVROT_OK;
 }
 
@@ -267,10 +291,10 @@ int launch_grouped(const __half* x16, const float* s_x, int64_t M, int64_t K,
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, w.Y, w.N, w.kchunk, in_scale};
+    lins[n++] = to_linear(w, w.Y, in_scale);
   }
   if (n == 0) return CONVROT_OK;
-  return launch_gemm(x16, s_x, M, K, lins, n, false, s, sync);
+  return launch_linears(x16, s_x, M, K, lins, n, false, s, sync);
 }
 
 }  // namespace convrot
@@ -328,7 +352,7 @@ int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, in
       const convrot_weight& w = weights[j];
       if (w.N == 0) continue;
       if (overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.Y, static_cast<size_t>(M) * w.N * 4) ||
-          overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.q16, static_cast<size_t>(w.N) * K * 2) ||
+          overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, weight_codes(w), weight_code_bytes(w, K)) ||
           (w.scale && overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.scale, w.N * 4)) ||
           (w.bias && overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.bias, w.N * 4)))
         return CONVROT_ERR_ALIAS;
@@ -455,8 +479,39 @@ int convrot_weight_chunks(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchu
 int convrot_device_status(void* stream) {
   if (int st = check_device()) return st;
   const int gemm_st = read_and_clear_device_error(static_cast<cudaStream_t>(stream));
+  const int w4_st = read_and_clear_w4_error();
   const int pack_st = read_and_clear_pack_error();
-  return gemm_st != CONVROT_OK ? gemm_st : pack_st;
+  return gemm_st != CONVROT_OK ? gemm_st : (w4_st != CONVROT_OK ? w4_st : pack_st);
+}
+
+size_t int8_gemm_s32_w4_workspace_size(int64_t M, int64_t K) {
+  if (M < 0 || K < 0) return 0;
+  return round256(static_cast<size_t>(M) * K * 2) + CONVROT_GEMM_SYNC_BYTES;
+}
+
+int int8_gemm_s32_w4(const int8_t* Q_x, int64_t M, int64_t K, const uint8_t* Q_w4, int64_t N, int32_t* A,
+                     void* workspace, size_t workspace_bytes, void* stream) {
+  if (M < 0 || N < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (M == 0 || N == 0) return CONVROT_OK;
+  if (!Q_x || !Q_w4 || !A) return CONVROT_ERR_ARG;
+  if (M > 0x7fffffff || N > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  if (K % 64 != 0 || !aligned16(Q_x) || !aligned16(Q_w4) || !aligned16(A) || (workspace && !aligned16(workspace)))
+    return CONVROT_ERR_ALIGN;
+  if (K > CONVROT_W4_MAX_K) return CONVROT_ERR_UNSUPPORTED;
+  const size_t need = int8_gemm_s32_w4_workspace_size(M, K);
+  if (!workspace || workspace_bytes < need) return CONVROT_ERR_WORKSPACE;
+  const size_t na = static_cast<size_t>(M) * N * 4, mk = static_cast<size_t>(M) * K, nk = static_cast<size_t>(N) * K / 2;
+  if (overlaps(A, na, Q_x, mk) || overlaps(A, na, Q_w4, nk) || overlaps(A, na, workspace, need) ||
+      overlaps(workspace, need, Q_x, mk) || overlaps(workspace, need, Q_w4, nk))
+    return CONVROT_ERR_ALIAS;
+  if (int st = check_device()) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  __half* x16 = reinterpret_cast<__half*>(ws);
+  if (int st = launch_widen(Q_x, x16, M * K, s)) return st;
+  GemmLinear lin{nullptr, nullptr, nullptr, A, N, nullptr};
+  lin.w4 = Q_w4;
+  return launch_gemm_w4(x16, nullptr, M, K, &lin, 1, true, s, sync_at(ws + need - CONVROT_GEMM_SYNC_BYTES));
 }
 
 }  // extern "C"

@@ -432,14 +432,31 @@ int launch_w4_expand(const uint8_t* src, int64_t n, int8_t* q8, __half* q16, cud
 int launch_widen(const int8_t* src, __half* dst, int64_t n, cudaStream_t stream);
 
 struct GemmLinear {
-  const __half* w16;   // [N,K] fp16 weight codes
+  const __half* w16;   // [N,K] fp16 weight codes, or null for packed 4-bit weights
   const float* s_w;    // [N] or null
   const float* bias;   // [N] or null
   void* out;           // [M,N] fp32 Y or int32 A
   int64_t N;
   const int32_t* kchunk;  // [ceil(N/128)] exact-chunk plan (64-wide K blocks per chunk) or null
   float in_scale = 1.0f;       // the activations were packed times this; Y is divided by it before the bias
+  const uint8_t* w4 = nullptr;  // [N,K/2] packed signed 4-bit weights (low nibble first), when w16 is null
 };
+
+// The GEMM operand of a weight descriptor (binary16 codes or packed 4-bit
+// weights) and the device bytes it spans.
+inline const void* weight_codes(const convrot_weight& w) {
+  return w.q16 ? static_cast<const void*>(w.q16) : static_cast<const void*>(w.q4);
+}
+inline size_t weight_code_bytes(const convrot_weight& w, int64_t K) {
+  return w.q16 ? static_cast<size_t>(w.N) * K * 2 : static_cast<size_t>(w.N) * K / 2;
+}
+// A weight descriptor as one linear of a GEMM launch, writing `out`.
+inline GemmLinear to_linear(const convrot_weight& w, void* out, float in_scale = 1.0f) {
+  GemmLinear l{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, out, w.N, w.q16 ? w.kchunk : nullptr,
+               in_scale};
+  l.w4 = w.q16 ? nullptr : w.q4;
+  return l;
+}
 
 // Exact-chunk plan of int8 weight codes (see convrot_weight_chunks).
 int launch_chunk_plan(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, cudaStream_t stream);
@@ -464,11 +481,28 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
                 const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
                 GemmSync sync = GemmSync());
 
+// The same for linears with packed 4-bit weights (w4): the S8 x S4 GEMM, which
+// reads the packed bytes. K % 64 == 0, K <= CONVROT_W4_MAX_K, N % 4 == 0
+// unless raw_s32.
+int launch_gemm_w4(const __half* x16, const float* s_x, int64_t M, int64_t K,
+                   const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
+                   GemmSync sync = GemmSync());
+
+// Every linear of the list, binary16-weight and packed 4-bit ones in one
+// launch each (in that order, on the same stream and hand-over words).
+int launch_linears(const __half* x16, const float* s_x, int64_t M, int64_t K,
+                   const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
+                   GemmSync sync = GemmSync());
+
+// Activation rows per tile (256, 192 or 128) for a grouped launch (gemm.cu).
+int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool can_split);
+
 // ---------------------------------------------------------------------------
 // host-side checks and the grouped launch shared by the entry points (api.cu)
 // ---------------------------------------------------------------------------
 
-// n_weights in [1, CONVROT_MAX_LINEARS]; every non-empty descriptor has q16 and Y.
+// n_weights in [1, CONVROT_MAX_LINEARS]; every non-empty descriptor has Y and
+// exactly one of q16, q4.
 int check_weight_list(const convrot_weight* weights, int n_weights);
 // Alignment and aliasing of the weight descriptors against each other and
 // against the activation-side arrays [in0, in0+n0) and [in1, in1+n1).

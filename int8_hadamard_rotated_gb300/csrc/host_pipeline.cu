@@ -118,9 +118,13 @@ extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, i
   for (int j = 0; j < n_weights; ++j) {
     const convrot_weight& w = weights[j];
     if (w.N == 0) continue;
-    if (!aligned16(w.q16) || (w.scale && !aligned16(w.scale)) || (w.bias && !aligned16(w.bias)))
+    if (!aligned16(weight_codes(w)) || (w.scale && !aligned16(w.scale)) || (w.bias && !aligned16(w.bias)))
       return CONVROT_ERR_ALIGN;
-    if (overlaps(workspace, need, w.q16, static_cast<size_t>(w.N) * K * 2) ||
+    if (w.q4) {
+      if (K % 64 != 0 || w.N % 4 != 0) return CONVROT_ERR_ALIGN;
+      if (K > CONVROT_W4_MAX_K) return CONVROT_ERR_UNSUPPORTED;
+    }
+    if (overlaps(workspace, need, weight_codes(w), weight_code_bytes(w, K)) ||
         overlaps(workspace, need, w.scale, static_cast<size_t>(w.N) * 4) ||
         overlaps(workspace, need, w.bias, static_cast<size_t>(w.N) * 4))
       return CONVROT_ERR_ALIAS;
@@ -165,11 +169,11 @@ extern "C" int convrot_linear_host(const void* X_host, int x_dtype, int64_t M, i
     for (int j = 0; j < n_weights; ++j) {
       const convrot_weight& w = weights[j];
       if (w.N == 0) continue;
-      lins[n++] = GemmLinear{reinterpret_cast<const __half*>(w.q16), w.scale, w.bias, B[b].y + off, w.N, w.kchunk};
+      lins[n++] = to_linear(w, B[b].y + off);
       off += static_cast<size_t>(m) * w.N;
     }
     if (n > 0)
-      if (int st = launch_gemm(B[b].q16, B[b].s_x, m, K, lins, n, false, s, sync)) return st;
+      if (int st = launch_linears(B[b].q16, B[b].s_x, m, K, lins, n, false, s, sync)) return st;
     CONVROT_TRY(cudaEventRecord(ev.done[b], s));
     // copy out every linear's rows of this chunk (contiguous in both places)
     CONVROT_TRY(cudaStreamWaitEvent(sout, ev.done[b], 0));

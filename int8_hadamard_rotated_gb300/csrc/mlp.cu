@@ -46,7 +46,8 @@ extern "C" int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int
   if (M < 0 || K <= 0) return CONVROT_ERR_ARG;
   if (x_dtype != CONVROT_F32 && x_dtype != CONVROT_F16) return CONVROT_ERR_ARG;
   if (activation != CONVROT_ACT_NONE && activation != CONVROT_ACT_GELU) return CONVROT_ERR_ARG;
-  if (!up || !down || up->N <= 0 || down->N <= 0 || !up->q16 || !down->q16 || !down->Y) return CONVROT_ERR_ARG;
+  if (!up || !down || up->N <= 0 || down->N <= 0 || !down->Y) return CONVROT_ERR_ARG;
+  if ((!up->q16) == (!up->q4) || (!down->q16) == (!down->q4)) return CONVROT_ERR_ARG;  // one kind of weight each
   if (M == 0) return CONVROT_OK;
   if (!X) return CONVROT_ERR_ARG;
   const int64_t N_up = up->N;
@@ -77,13 +78,12 @@ extern "C" int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int
   __half* h16 = reinterpret_cast<__half*>(ws + l.h16);
   float* s_h = reinterpret_cast<float*>(ws + l.s_h);
   if (int st = launch_pack(X, x_dtype, M, K, G_up, x16, kPackF16, s_x, s)) return st;
-  GemmLinear lu{reinterpret_cast<const __half*>(up->q16), up->scale, up->bias, H, N_up, up->kchunk};
+  const GemmLinear lu = to_linear(*up, H);
   const GemmSync sync = sync_at(ws + l.sync);  // the two GEMMs run one after the other
-  if (int st = launch_gemm(x16, s_x, M, K, &lu, 1, false, s, sync)) return st;
+  if (int st = launch_linears(x16, s_x, M, K, &lu, 1, false, s, sync)) return st;
   int st = (activation == CONVROT_ACT_GELU) ? launch_pack_gelu(H, M, N_up, G_down, h16, s_h, s)
                                              : launch_pack(H, CONVROT_F32, M, N_up, G_down, h16, kPackF16, s_h, s);
   if (st) return st;
-  GemmLinear ld{reinterpret_cast<const __half*>(down->q16), down->scale, down->bias, down->Y, down->N,
-                down->kchunk};
-  return launch_gemm(h16, s_h, M, N_up, &ld, 1, false, s, sync);
+  const GemmLinear ld = to_linear(*down, down->Y);
+  return launch_linears(h16, s_h, M, N_up, &ld, 1, false, s, sync);
 }

@@ -40,6 +40,7 @@ F16 = 1
 MAX_LINEARS = 8
 PACK_MAX_K = 32768
 MAX_K = 133144
+W4_MAX_K = 16384
 CHUNK_ROWS = 128
 NOALLOC_SCRATCH_BYTES = 32 << 20
 GEMM_SYNC_BYTES = 4096
@@ -63,7 +64,8 @@ class convrot_prologue(ctypes.Structure):
 class convrot_weight(ctypes.Structure):
     _fields_ = [("q16", ctypes.c_void_p), ("scale", ctypes.c_void_p),
                 ("bias", ctypes.c_void_p), ("N", ctypes.c_int64),
-                ("Y", ctypes.c_void_p), ("kchunk", ctypes.c_void_p)]
+                ("Y", ctypes.c_void_p), ("kchunk", ctypes.c_void_p),
+                ("q4", ctypes.c_void_p)]
 
 
 _LIB = None
@@ -85,6 +87,8 @@ SIGNATURES = {
     "convrot_linear_scaled": (_I, [_VP, _I, _I64, _I64, _I, ctypes.c_float, ctypes.POINTER(convrot_weight), _I,
                                    _VP, _SZ, _VP]),
     "int8_gemm_s32": (_I, [_VP, _I64, _I64, _VP, _VP, _VP, _I64, _VP, _VP, _SZ, _VP]),
+    "int8_gemm_s32_w4_workspace_size": (_SZ, [_I64, _I64]),
+    "int8_gemm_s32_w4": (_I, [_VP, _I64, _I64, _VP, _I64, _VP, _VP, _SZ, _VP]),
     "convrot_weight_chunks": (_I, [_VP, _I64, _I64, _VP, _VP]),
     "convrot_w4_expand": (_I, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
@@ -261,15 +265,38 @@ def int8_gemm_s32(Q_x, Q_w=None, Q_w16=None, A=None, workspace=None, stream=None
     return A
 
 
+def int8_gemm_s32_w4(Q_x, Q_w4, A=None, workspace=None, stream=None) -> torch.Tensor:
+    """Raw int32 A = Q_x Q_w^T with packed signed 4-bit weights Q_w4 [N, K/2]
+    (uint8, low nibble first), through the S8 x S4 GEMM."""
+    _need(Q_x, torch.int8, "Q_x")
+    _need(Q_w4, torch.uint8, "Q_w4")
+    M, K = Q_x.shape
+    N = Q_w4.shape[0]
+    if Q_w4.shape[1] * 2 != K:
+        raise ValueError("Q_w4 must be [N, K/2]")
+    if A is None:
+        A = torch.empty((M, N), dtype=torch.int32, device=Q_x.device)
+    ws = _workspace(int(lib().int8_gemm_s32_w4_workspace_size(M, K)), Q_x.device, workspace)
+    _check(lib().int8_gemm_s32_w4(_ptr(Q_x), M, K, _ptr(Q_w4), N, _ptr(A), _ptr(ws), ws.numel(), _stream(stream)),
+           "int8_gemm_s32_w4")
+    return A
+
+
 def make_weights(q16s: Sequence[torch.Tensor], scales: Sequence[Optional[torch.Tensor]],
                  biases: Sequence[Optional[torch.Tensor]], Ys: Sequence[torch.Tensor],
                  kchunks: Optional[Sequence[Optional[torch.Tensor]]] = None):
-    """The convrot_weight descriptors (kchunks: optional exact-chunk plans)."""
+    """The convrot_weight descriptors (kchunks: optional exact-chunk plans).
+    Each weight is binary16 codes [N, K] (float16) or packed signed 4-bit
+    weights [N, K/2] (uint8, low nibble first), which the S8 x S4 GEMM reads
+    as they are."""
     arr = (convrot_weight * len(q16s))()
     if kchunks is None:
         kchunks = [None] * len(q16s)
     for j, (q, s, b, y, kc) in enumerate(zip(q16s, scales, biases, Ys, kchunks)):
-        arr[j] = convrot_weight(_ptr(q), _ptr(s), _ptr(b), q.shape[0], _ptr(y), _ptr(kc))
+        if q.dtype == torch.uint8:
+            arr[j] = convrot_weight(None, _ptr(s), _ptr(b), q.shape[0], _ptr(y), None, _ptr(q))
+        else:
+            arr[j] = convrot_weight(_ptr(q), _ptr(s), _ptr(b), q.shape[0], _ptr(y), _ptr(kc), None)
     return arr
 
 
@@ -430,8 +457,9 @@ def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: 
                 Y: Optional[torch.Tensor] = None, H: Optional[torch.Tensor] = None, workspace=None,
                 stream=None) -> torch.Tensor:
     """Up linear, activation, down linear on the device. `up` and `down` are
-    (q16, scale, bias, kchunk) tuples; H (optional, fp32 [M, N_up]) receives
-    the up linear's output before the activation."""
+    (weight codes, scale, bias, kchunk) tuples, the codes binary16 [N, K] or
+    packed 4-bit [N, K/2] (uint8); H (optional, fp32 [M, N_up]) receives the
+    up linear's output before the activation."""
     xd = _xdtype(X)
     _need(X, X.dtype, "X")
     M, K = X.shape
@@ -442,8 +470,8 @@ def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: 
         Y = torch.empty((M, N_down), dtype=torch.float32, device=X.device)
     if H is not None:
         _need(H, torch.float32, "H")
-    wu = (convrot_weight * 1)(convrot_weight(_ptr(uq), _ptr(us), _ptr(ub), N_up, _ptr(H), _ptr(uk)))
-    wd = (convrot_weight * 1)(convrot_weight(_ptr(dq), _ptr(ds), _ptr(db), N_down, _ptr(Y), _ptr(dk)))
+    wu = make_weights([uq], [us], [ub], [H], [uk])
+    wd = make_weights([dq], [ds], [db], [Y], [dk])
     ws = _workspace(convrot_mlp_workspace_size(M, K, N_up), X.device, workspace)
     _check(lib().convrot_mlp(_ptr(X), xd, M, K, G_up, wu, activation, G_down, wd, _ptr(ws), ws.numel(),
                              _stream(stream)), "convrot_mlp")

@@ -169,3 +169,38 @@ def test_scaled_linear_rejects_bad_scales(L):
     f = L.convrot_linear_scaled
     for a in (0.0, -1.0, float("inf"), float("nan")):
         assert f(A0, ops.F32, 16, 256, 256, a, ws, 1, A5, 1 << 40, None) == ops.ERR_ARG
+
+
+def test_w4_descriptor_checks(L):
+    """A weight descriptor holds exactly one kind of weight (binary16 codes or
+    packed 4-bit bytes); a packed 4-bit linear needs K % 64 == 0, N % 4 == 0
+    and K <= CONVROT_W4_MAX_K. All checked before any device call."""
+    from int8_hadamard_rotated_gb300 import ops
+    W = ops.convrot_weight
+    f = L.convrot_linear
+    big = 1 << 40
+    both = (W * 1)(W(A1, None, None, 64, A4, None, A2))
+    neither = (W * 1)(W(None, None, None, 64, A4, None, None))
+    q4 = (W * 1)(W(None, A2, A3, 64, A4, None, A1))
+    assert f(A0, ops.F32, 16, 256, 256, both, 1, A5, big, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 256, 256, neither, 1, A5, big, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 96, 16, q4, 1, A5, big, None) == ops.ERR_ALIGN          # K % 64
+    odd_n = (W * 1)(W(None, None, None, 66, A4, None, A1))
+    assert f(A0, ops.F32, 16, 256, 256, odd_n, 1, A5, big, None) == ops.ERR_ALIGN     # N % 4
+    assert f(A0, ops.F32, 16, 16384 + 1024, 1024, q4, 1, A5, big, None) == ops.ERR_UNSUPPORTED
+    assert f(A0, ops.F32, 16, 256, 256, (W * 1)(W(None, None, None, 64, A4, None, A1 + 8)), 1, A5, big,
+             None) == ops.ERR_ALIGN                                                     # unaligned bytes
+    # the packed bytes span N * K / 2: an output placed right after them is fine,
+    # one byte earlier overlaps
+    after = (W * 1)(W(None, None, None, 64, A1 + 64 * 128, None, A1))
+    assert f(A0, ops.F32, 16, 256, 256, after, 1, A5, big, None) == ops.ERR_DEVICE or \
+        f(A0, ops.F32, 16, 256, 256, after, 1, A5, big, None) == ops.OK
+    inside = (W * 1)(W(None, None, None, 64, A1 + 64 * 128 - 16, None, A1))
+    assert f(A0, ops.F32, 16, 256, 256, inside, 1, A5, big, None) == ops.ERR_ALIAS
+    g = L.int8_gemm_s32_w4
+    assert L.int8_gemm_s32_w4_workspace_size(16, 256) == 16 * 256 * 2 + ops.GEMM_SYNC_BYTES
+    assert g(A0, 16, 96, A1, 64, A2, A3, big, None) == ops.ERR_ALIGN
+    assert g(A0, 16, 16384 + 64, A1, 64, A2, A3, big, None) == ops.ERR_UNSUPPORTED
+    assert g(A0, 16, 256, A1, 64, A2, A3, 100, None) == ops.ERR_WORKSPACE
+    assert g(A0, 16, 256, A1, 64, A1 + 64, A3, big, None) == ops.ERR_ALIAS
+    assert g(A0, 0, 256, A1, 64, A2, A3, big, None) == ops.OK
