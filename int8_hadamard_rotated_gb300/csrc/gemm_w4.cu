@@ -21,17 +21,17 @@
 // warps per CTA and three rings of shared-memory slots, each stepped once per
 // 64-deep K block:
 //   activation ring (6-8 slots): binary16 activation codes, loaded by the pair
-//     TMA of warp 8 as soon as the MMAs release a slot;
+//     TMA of warp 15 as soon as the MMAs release a slot;
 //   packed ring (8 slots): the CTA's 128 rows of packed weight bytes (4 KB per
-//     block), loaded by warp 10 up to 8 blocks ahead;
+//     block), loaded by warp 8 up to 8 blocks ahead;
 //   weight ring (4 slots): the binary16 weight tile (16 KB, 128-byte swizzle,
 //     the layout a tensor-map load of binary16 codes would give), written by
-//     the converter warps 11-18 in four pairs. Pair q widens every block
+//     the eight converter warps (9, 10, 12-14, 16-18) in four pairs. Pair q widens every block
 //     whose index in the CTA's block stream is q modulo 4, each warp half of
 //     its rows, so four blocks are in conversion at once and the latency of
 //     each (its shared-memory stores must drain before the proxy fence lets
 //     the tensor cores read them) overlaps the others.
-//   warp 9      MMA issuer (the even CTA): once a block's activation slot is
+//   warp 11     MMA issuer (the even CTA): once a block's activation slot is
 //               full and both CTAs' converter warps have signalled its weight
 //               slot, tcgen05.mma kind::f16 (M = 256, N = BN) into one of two
 //               TMEM accumulators; the commits release both slots in both CTAs.
@@ -59,21 +59,41 @@ namespace {
 using namespace gemm;
 
 constexpr int CONV_WARPS = 8;                     // four pairs, one K block per pair, round-robin
-constexpr int X_PRODUCER_WARP = NUM_EPI_WARPS;     // 8
-constexpr int W4_MMA_WARP = NUM_EPI_WARPS + 1;     // 9
-constexpr int PK_PRODUCER_WARP = NUM_EPI_WARPS + 2;  // 10
-constexpr int CONV_WARP0 = NUM_EPI_WARPS + 3;      // 11
-constexpr int W4_THREADS = (CONV_WARP0 + CONV_WARPS) * 32;
+// Warp roles. Warp w issues on scheduler w mod 4. The MMA issuer paces the
+// whole kernel, so it shares its scheduler only with light warps (two
+// epilogue warps, which idle between tiles, and the activation loader); the
+// converters' bursts of widening arithmetic run on the other three.
+constexpr int W4_WARPS = NUM_EPI_WARPS + 3 + CONV_WARPS;  // 19
+constexpr int W4_MMA_WARP = 11;        // scheduler 3
+constexpr int X_PRODUCER_WARP = 15;    // scheduler 3
+constexpr int PK_PRODUCER_WARP = 8;    // scheduler 0
+constexpr int W4_THREADS = W4_WARPS * 32;
+__host__ __device__ constexpr bool conv_slot(int w) {
+  return w >= NUM_EPI_WARPS && w < W4_WARPS && w != W4_MMA_WARP && w != X_PRODUCER_WARP && w != PK_PRODUCER_WARP;
+}
+// Index of converter warp w among the converter warps (0 .. CONV_WARPS - 1).
+__host__ __device__ constexpr int conv_index(int w) {
+  int i = 0;
+  for (int v = NUM_EPI_WARPS; v < w; ++v) i += conv_slot(v) ? 1 : 0;
+  return i;
+}
+static_assert(conv_index(W4_WARPS) == CONV_WARPS, "every remaining warp converts");
+static_assert((W4_MMA_WARP & 3) == (X_PRODUCER_WARP & 3) && (W4_MMA_WARP & 3) != (PK_PRODUCER_WARP & 3),
+              "no converter shares the MMA warp's scheduler");
 constexpr int PW_BYTES = CTA_M * BK / 2;  // packed weight bytes of one CTA per K block (4 KB)
 constexpr int W4_TILE_M = 2 * CTA_M;
 constexpr int CONV_PAIRS = CONV_WARPS / 2;  // pair q widens the blocks q (mod CONV_PAIRS)
 constexpr int W_SLOTS = CONV_PAIRS;         // binary16 weight ring: slot q belongs to pair q
 constexpr int PK_SLOTS = 2 * CONV_PAIRS;    // packed ring (prefetch depth): slots q, q + CONV_PAIRS for pair q
+constexpr int DONE_SLOTS = 8;               // "block done" ring: one MMA commit per block
 
 static_assert(127 * 8 * CONVROT_W4_MAX_K < (1 << 24), "one tile must stay exact in fp32");
 static_assert(PW_BYTES % (2 * 32 * 16) == 0, "a converter warp widens whole 16-byte chunks per lane");
-static_assert(W_SLOTS % CONV_PAIRS == 0 && PK_SLOTS % CONV_PAIRS == 0,
+static_assert(W_SLOTS % CONV_PAIRS == 0 && PK_SLOTS % CONV_PAIRS == 0 && DONE_SLOTS % CONV_PAIRS == 0,
               "every slot is waited on by one converter pair only, in order");
+static_assert((DONE_SLOTS & (DONE_SLOTS - 1)) == 0 && (CONV_PAIRS & (CONV_PAIRS - 1)) == 0 &&
+                  (PK_SLOTS & (PK_SLOTS - 1)) == 0,
+              "ring indices by masks");
 
 template <int BN_>
 struct GeomW4 {
@@ -94,8 +114,8 @@ struct GeomW4 {
   static constexpr int SMEM_YOUT = SMEM_PW + PK_SLOTS * PW_BYTES;      // [2][2][Y_ROWS][128] fp32
   static constexpr int SMEM_SX = SMEM_YOUT + 2 * Y_HALF_BYTES;         // [2][128] fp32 row scales
   static constexpr int SMEM_BARS = SMEM_SX + 2 * 128 * 4;
-  // x_full, x_empty [X]; w_full, w_empty [W]; pk_full, pk_empty [PK]; tfull, tempty [2]; drain
-  static constexpr int NUM_BARS = 2 * X_SLOTS + 2 * W_SLOTS + 2 * PK_SLOTS + 2 + 2 + 1;
+  // x_full [X]; w_full [W]; done [DONE]; pk_full, pk_empty [PK]; tfull, tempty [2]; drain
+  static constexpr int NUM_BARS = X_SLOTS + W_SLOTS + DONE_SLOTS + 2 * PK_SLOTS + 2 + 2 + 1;
   static constexpr int SMEM_MISC = SMEM_BARS + NUM_BARS * 8;           // tmem base (u32), abort flag (int)
   static constexpr int SMEM_ALLOC = SMEM_MISC + 16 + 1024;
 };
@@ -107,35 +127,6 @@ static_assert(GeomW4<256>::X_SLOTS >= 5 && GeomW4<256>::SMEM_ALLOC <= 227 * 1024
 // CTA-scope release (see the kernel description).
 __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
-}
-
-// Wait for a phase of an mbarrier that other CTAs of the cluster arrive on
-// (acquire at cluster scope, so their shared-memory writes are visible).
-// Bounded like mbar_wait.
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok) : "r"(smem_u32(bar)), "r"(parity) : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  int* err_word) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if ((it & 63) == 63) {
-      if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
-        if (abort_flag) *abort_flag = 1;
-        record_error(err_word, CONVROT_ERR_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 // Eight signed 4-bit values (one 32-bit word of the packed row, element 2j in
@@ -171,10 +162,9 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
   constexpr int XS = Gm::X_SLOTS;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Gm::SMEM_BARS);
   uint64_t* x_full = bars;                          // [XS] (even CTA: both CTAs' activation bytes)
-  uint64_t* x_empty = x_full + XS;                  // [XS] the pair's MMAs released the slot
-  uint64_t* w_full = x_empty + XS;                  // [W_SLOTS] (even CTA: one converter warp of each CTA)
-  uint64_t* w_empty = w_full + W_SLOTS;             // [W_SLOTS] the pair's MMAs released the slot
-  uint64_t* pk_full = w_empty + W_SLOTS;            // [PK_SLOTS] this CTA's packed bytes landed
+  uint64_t* w_full = x_full + XS;                   // [W_SLOTS] (even CTA: the converter pairs of both CTAs)
+  uint64_t* done = w_full + W_SLOTS;                // [DONE_SLOTS] the pair's MMAs of block n finished (n mod 8)
+  uint64_t* pk_full = done + DONE_SLOTS;            // [PK_SLOTS] this CTA's packed bytes landed
   uint64_t* pk_empty = pk_full + PK_SLOTS;          // [PK_SLOTS] this CTA's converter read them
   uint64_t* tfull = pk_empty + PK_SLOTS;            // [2]
   uint64_t* tempty = tfull + 2;                     // [2]
@@ -192,14 +182,9 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
   constexpr uint16_t pair_mask = 0x3u;
 
   if (threadIdx.x == X_PRODUCER_WARP * 32) {
-    for (int s = 0; s < XS; ++s) {
-      mbar_init(&x_full[s], 1);
-      mbar_init(&x_empty[s], 1);
-    }
-    for (int s = 0; s < W_SLOTS; ++s) {
-      mbar_init(&w_full[s], 4);   // the two warps of a converter pair in each CTA
-      mbar_init(&w_empty[s], 1);
-    }
+    for (int s = 0; s < XS; ++s) mbar_init(&x_full[s], 1);
+    for (int s = 0; s < W_SLOTS; ++s) mbar_init(&w_full[s], 4);  // the two warps of a converter pair in each CTA
+    for (int s = 0; s < DONE_SLOTS; ++s) mbar_init(&done[s], 1);
     for (int s = 0; s < PK_SLOTS; ++s) {
       mbar_init(&pk_full[s], 1);
       mbar_init(&pk_empty[s], 2);  // the two warps of this CTA's converter pair
@@ -234,8 +219,9 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       const bool is_x = (warp == X_PRODUCER_WARP);
       const uint64_t pol = l2_policy_evict_normal();
       const uint32_t x_full_leader = mapa_shared(smem_u32(x_full), 0);
-      const int slots = is_x ? XS : PK_SLOTS;
-      uint32_t n = 0;  // block index in this CTA's stream
+      const uint32_t slots = is_x ? XS : PK_SLOTS;
+      uint32_t n = 0;           // block index in this CTA's stream
+      uint32_t s = 0, ph = 0;   // its slot and the slot's use parity
       bool ok = true;
       WorkItem it;
       for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
@@ -243,9 +229,12 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
         const int w_row = c.wt * W4_TILE_M + static_cast<int>(rank) * CTA_M;
         const int x_row = c.xt * BN + static_cast<int>(rank) * Gm::X_ROWS;
         for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
-          const uint32_t s = n % slots, ph = (n / slots) & 1u;
           if (is_x) {
-            if (!mbar_wait(&x_empty[s], ph ^ 1u, abort_flag, err)) { ok = false; break; }
+            // the slot is free once the MMAs of block n - XS have finished
+            if (n >= slots) {
+              const uint32_t m = n - slots;
+              if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+            }
             if (leader) mbar_arrive_expect_tx(&x_full[s], 2 * Gm::X_BYTES);
             tma_load_2d_pair(smem + Gm::SMEM_X + s * Gm::X_BYTES, &p.tmap_x, x_full_leader + s * 8u, kb * BK,
                              x_row, pol);
@@ -255,21 +244,25 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
             tma_load_2d(smem + Gm::SMEM_PW + s * PW_BYTES, &p.tmap_w[c.lin], &pk_full[s], kb * (BK / 2), w_row,
                         pol);
           }
+          if (++s == slots) { s = 0; ph ^= 1u; }
         }
       }
       // no copy may land after the CTAs exit: wait (bounded) for the last
       // phase of every slot that was filled
-      for (uint32_t s = 0; s < static_cast<uint32_t>(slots); ++s)
-        if (n > s) {
-          const uint32_t ph = ((n - 1 - s) / slots) & 1u;
-          if (!is_x) mbar_wait(&pk_full[s], ph, nullptr, err);
-          else if (leader) mbar_wait(&x_full[s], ph, nullptr, err);
+      for (uint32_t t = 0; t < slots; ++t)
+        if (n > t) {
+          const uint32_t tph = ((n - 1 - t) / slots) & 1u;
+          if (!is_x) mbar_wait(&pk_full[t], tph, nullptr, err);
+          else if (leader) mbar_wait(&x_full[t], tph, nullptr, err);
         }
     }
     __syncwarp();
   } else if (warp == W4_MMA_WARP) {
     if (lane == 0 && leader) {
-      uint32_t n = 0, acc_iter = 0;
+      uint32_t acc_iter = 0;
+      uint32_t xs = 0, xph = 0, ws = 0, wph = 0, ds = 0;  // ring positions of the next block
+      const uint64_t a_desc0 = smem_desc_sw128(smem_u32(smem + Gm::SMEM_W));
+      const uint64_t b_desc0 = smem_desc_sw128(smem_u32(smem + Gm::SMEM_X));
       bool ok = true;
       WorkItem it;
       for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
@@ -278,20 +271,22 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
         if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
-        for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
-          const uint32_t xs = n % XS, ws = n % W_SLOTS;
-          if (!mbar_wait(&x_full[xs], (n / XS) & 1u, abort_flag, err)) { ok = false; break; }
-          if (!mbar_wait_cluster(&w_full[ws], (n / W_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+        for (int kb = it.kb0; kb < it.kb1; ++kb) {
+          if (!mbar_wait(&x_full[xs], xph, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait(&w_full[ws], wph, abort_flag, err)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t a_desc = smem_desc_sw128(smem_u32(smem + Gm::SMEM_W + ws * Gm::W_BYTES));
-          const uint64_t b_desc = smem_desc_sw128(smem_u32(smem + Gm::SMEM_X + xs * Gm::X_BYTES));
+          // descriptors advance by the slot offset (address >> 4 in the low field)
+          const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(ws * (Gm::W_BYTES >> 4));
+          const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(xs * (Gm::X_BYTES >> 4));
 #pragma unroll
           for (int k = 0; k < BK / UMMA_K; ++k) {
             const uint64_t koff = static_cast<uint64_t>((k * UMMA_K * 2) >> 4);
             mma_f16_ss_pair(d_tmem, a_desc + koff, b_desc + koff, Gm::IDESC, (kb > it.kb0 || k > 0) ? 1u : 0u);
           }
-          mma_commit_pair(&x_empty[xs], pair_mask);
-          mma_commit_pair(&w_empty[ws], pair_mask);
+          mma_commit_pair(&done[ds], pair_mask);
+          if (++xs == static_cast<uint32_t>(XS)) { xs = 0; xph ^= 1u; }
+          if (++ws == static_cast<uint32_t>(W_SLOTS)) { ws = 0; wph ^= 1u; }
+          ds = (ds + 1) & (DONE_SLOTS - 1);
         }
         if (!ok) break;
         mma_commit_pair(&tfull[buf], pair_mask);
@@ -302,7 +297,7 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       mbar_wait(drain, 0, nullptr, err);
     }
     __syncwarp();
-  } else if (warp >= CONV_WARP0) {
+  } else if (conv_slot(warp)) {
     // ---------------------------- converters -------------------------------
     // Converter pair q (warps q and q + CONV_PAIRS) widens the blocks
     // n = q (mod CONV_PAIRS) of this CTA's stream, always into weight slot q,
@@ -313,7 +308,7 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
     // elements 32 (c & 1) .. +31 of weight row c >> 1, which become the row's
     // binary16 chunks 4 (c & 1) .. +3 (8 elements each) at their
     // 128-byte-swizzle positions.
-    const int cw = warp - CONV_WARP0;
+    const int cw = conv_index(warp);
     const uint32_t q = static_cast<uint32_t>(cw % CONV_PAIRS);
     const int hr = cw / CONV_PAIRS;
     const uint32_t w_full_leader = mapa_shared(smem_u32(w_full), 0);
@@ -322,30 +317,45 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
     WorkItem it;
     for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
       for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
-        if (n % CONV_PAIRS != q) continue;
-        const uint32_t ps = n % PK_SLOTS, ws = n % W_SLOTS;
+        if ((n & (CONV_PAIRS - 1)) != q) continue;
+        const uint32_t ps = n & (PK_SLOTS - 1), ws = n % W_SLOTS;
         if (!mbar_wait(&pk_full[ps], (n / PK_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
-        if (!mbar_wait(&w_empty[ws], ((n / W_SLOTS) & 1u) ^ 1u, abort_flag, err)) { ok = false; break; }
+        // widen into registers first (off the weight slot's critical path),
+        // hand the packed slot back, then store once the weight slot is free
+        constexpr int NCH = PW_BYTES / (2 * 32 * 16);  // 16-byte chunks per lane
         const uint8_t* spw = smem + Gm::SMEM_PW + ps * PW_BYTES;
+        uint32_t h[NCH][16];
+#pragma unroll
+        for (int i = 0; i < NCH; ++i) {
+          const int c = (PW_BYTES / 32) * hr + lane + 32 * i;
+          const uint4 in = *reinterpret_cast<const uint4*>(spw + 16 * c);
+          widen_w4x8(in.x, *reinterpret_cast<uint32_t(*)[4]>(&h[i][0]));
+          widen_w4x8(in.y, *reinterpret_cast<uint32_t(*)[4]>(&h[i][4]));
+          widen_w4x8(in.z, *reinterpret_cast<uint32_t(*)[4]>(&h[i][8]));
+          widen_w4x8(in.w, *reinterpret_cast<uint32_t(*)[4]>(&h[i][12]));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pk_empty[ps]);  // the packed bytes are in registers: reload the slot
+        // the weight slot is free once the MMAs of block n - W_SLOTS have finished
+        if (n >= static_cast<uint32_t>(W_SLOTS)) {
+          const uint32_t m = n - W_SLOTS;
+          if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+        }
         uint8_t* sw = smem + Gm::SMEM_W + ws * Gm::W_BYTES;
 #pragma unroll
-        for (int i = 0; i < PW_BYTES / (2 * 32 * 16); ++i) {
+        for (int i = 0; i < NCH; ++i) {
           const int c = (PW_BYTES / 32) * hr + lane + 32 * i;
           const int r = c >> 1, hpart = c & 1;
-          const uint4 in = *reinterpret_cast<const uint4*>(spw + 16 * c);
-          const uint32_t words[4] = {in.x, in.y, in.z, in.w};
 #pragma unroll
           for (int m = 0; m < 4; ++m) {
-            uint32_t h[4];
-            widen_w4x8(words[m], h);
             const int chunk = (4 * hpart + m) ^ (r & 7);
-            *reinterpret_cast<uint4*>(sw + r * 128 + chunk * 16) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(sw + r * 128 + chunk * 16) =
+                make_uint4(h[i][4 * m], h[i][4 * m + 1], h[i][4 * m + 2], h[i][4 * m + 3]);
           }
         }
         fence_proxy_async_smem();  // the tensor cores read this tile through the async proxy
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&pk_empty[ps]);  // the packed bytes are in registers/written out: reload the slot
           if (leader) mbar_arrive(&w_full[ws]);
           else mbar_arrive_remote_cta(w_full_leader + ws * 8u);
         }
