@@ -490,33 +490,7 @@ def run_gpu(args, rank, world, local_rank):
     del Xl, Ql, sl
 
     # ---- the DiT MLP pair on the device (convrot_mlp) ---------------------
-    mw = workloads.get("dit_mlp")
-    mcase = workloads.make_case(mw)
-    Xm = torch.from_numpy(mcase.X).to(dev)
-    mlp_w = []
-    for W, b in zip(mcase.Ws, mcase.bs):
-        q8, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), mw.G)
-        mlp_w.append((q16, s_w, torch.from_numpy(b).to(dev), ops.convrot_weight_chunks(q8)))
-        del q8
-    Ym = torch.empty((mw.M, mw.Ns[1]), dtype=torch.float32, device=dev)
-    wsm = torch.empty((ops.convrot_mlp_workspace_size(mw.M, mw.K, mw.Ns[0]),), dtype=torch.uint8, device=dev)
-    for _ in range(3):
-        ops.convrot_mlp(Xm, mw.G, mlp_w[0], ops.ACT_GELU, mw.G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
-    mt = []
-    for _ in range(10):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        ops.convrot_mlp(Xm, mw.G, mlp_w[0], ops.ACT_GELU, mw.G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
-        b.record(stream)
-        mt.append((a, b))
-    torch.cuda.synchronize()
-    mms = float(np.mean([a.elapsed_time(b) for a, b in mt]))
-    mlp = {"workload": f"dit_mlp: X fp32 [{mw.M},{mw.K}] -> up [{mw.Ns[0]},{mw.K}] + GELU -> repack -> "
-                       f"down [{mw.Ns[1]},{mw.Ns[0]}], G={mw.G}, one convrot_mlp call",
-           "ms": round(mms, 4), "TOPS": round(mw.gemm_ops / (mms * 1e-3) / 1e12, 2),
-           "ops_per_call": int(mw.gemm_ops)}
-    del Xm, mlp_w, Ym, wsm
+    mlp = mlp_leg(dev, flush, peak_tf, hbm, peak_kind, with_cpu=(world == 1 and rank == 0 and not args.no_cpu_baseline))
 
     nxt = next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step)
 
@@ -577,6 +551,162 @@ def run_gpu(args, rank, world, local_rank):
     if small is not None:
         result["small_configs_in_graph"] = small
     return result, case, w
+
+
+def mlp_leg(dev, flush, peak_tf, hbm, peak_kind, with_cpu=True, reps=10):
+    """The DiT MLP pair (X fp32 [4608, 3072] -> up [12288, 3072] -> GELU ->
+    down [3072, 12288], G = 256) as a leg of its own: the whole convrot_mlp
+    call, its four launches timed alone (the pack, the up GEMM with GELU in
+    its epilogue, the repack of H, the down GEMM; and the other placement of
+    GELU, a plain up GEMM and the repack with GELU), the rooflines of the two
+    GEMMs (tensor) and of the repack (HBM, on the algorithmic bytes: fp32 H
+    in, int8 codes and row scales out), the call end to end with host
+    buffers, the split-SwiGLU pair (gate and up [12288, 3072] sharing the
+    pack), and the oracle chain on a row sample of the host cores. L2 is
+    flushed before every timed launch; CUDA events on the launching stream."""
+    import torch
+    from int8_hadamard_rotated_gb300 import ops
+    stream = torch.cuda.current_stream()
+    sp = stream.cuda_stream
+    L = ops.lib()
+    mw = workloads.get("dit_mlp")
+    mcase = workloads.make_case(mw)
+    M, K, N_up, N_down, G = mw.M, mw.K, mw.Ns[0], mw.Ns[1], mw.G
+    Xm = torch.from_numpy(mcase.X).to(dev)
+    mlp_w = []
+    for W, b in zip(mcase.Ws, mcase.bs):
+        q8, s_w, q16 = ops.convrot_prepare_weight(torch.from_numpy(W).to(dev), G)
+        mlp_w.append((q16, s_w, torch.from_numpy(b).to(dev), ops.convrot_weight_chunks(q8)))
+        del q8
+    Ym = torch.empty((M, N_down), dtype=torch.float32, device=dev)
+    wsm = torch.empty((ops.convrot_mlp_workspace_size(M, K, N_up),), dtype=torch.uint8, device=dev)
+
+    def timed(fn, n=reps):
+        for _ in range(3):
+            fn()
+        ev = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in ev])) * 1e3  # us
+
+    chain = lambda: ops.convrot_mlp(Xm, G, mlp_w[0], ops.ACT_GELU, G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
+    t_chain = timed(chain)
+    ops_up = 2.0 * M * N_up * K
+    ops_down = 2.0 * M * N_down * N_up
+
+    # the four launches alone, on the same buffers
+    Qx = torch.empty((M, K), dtype=torch.float16, device=dev)
+    sx = torch.empty((M,), dtype=torch.float32, device=dev)
+    H = torch.empty((M, N_up), dtype=torch.float32, device=dev)
+    Qh = torch.empty((M, N_up), dtype=torch.float16, device=dev)
+    sh = torch.empty((M,), dtype=torch.float32, device=dev)
+    sync_ws = torch.zeros((ops.GEMM_SYNC_BYTES,), dtype=torch.uint8, device=dev)
+    wup = ops.make_weights([mlp_w[0][0]], [mlp_w[0][1]], [mlp_w[0][2]], [H], [mlp_w[0][3]])
+    wdn = ops.make_weights([mlp_w[1][0]], [mlp_w[1][1]], [mlp_w[1][2]], [Ym], [mlp_w[1][3]])
+
+    def chk(st, what):
+        if st:
+            raise ops.ConvrotError(st, what)
+    t_pack = timed(lambda: chk(L.convrot_pack_activations_f16(Xm.data_ptr(), ops.F32, M, K, G, Qx.data_ptr(),
+                                                               sx.data_ptr(), sp), "pack"))
+    t_up = timed(lambda: chk(L.convrot_linear_packed_act(Qx.data_ptr(), sx.data_ptr(), M, K, wup, 1, ops.ACT_GELU,
+                                                         sync_ws.data_ptr(), ops.GEMM_SYNC_BYTES, sp), "up GEMM + GELU"))
+    t_repack = timed(lambda: chk(L.convrot_pack_activations_f16(H.data_ptr(), ops.F32, M, N_up, G, Qh.data_ptr(),
+                                                                 sh.data_ptr(), sp), "repack"))
+    # the other placement of GELU: in the repack (convrot_pack_gelu_f16), after a plain up GEMM
+    t_up_plain = timed(lambda: chk(L.convrot_linear_packed(Qx.data_ptr(), sx.data_ptr(), M, K, wup, 1,
+                                                           sync_ws.data_ptr(), ops.GEMM_SYNC_BYTES, sp), "up GEMM"))
+    t_gelu_repack = timed(lambda: chk(L.convrot_pack_gelu_f16(H.data_ptr(), M, N_up, G, Qh.data_ptr(), sh.data_ptr(),
+                                                              sp), "GELU repack"))
+    t_down = timed(lambda: chk(L.convrot_linear_packed(Qh.data_ptr(), sh.data_ptr(), M, N_up, wdn, 1,
+                                                       sync_ws.data_ptr(), ops.GEMM_SYNC_BYTES, sp), "down GEMM"))
+    repack_bytes = M * N_up * 4 + M * N_up + M * 4   # algorithmic: fp32 H in, int8 codes + fp32 scales out
+    tf = lambda ops_, us: ops_ / (us * 1e-6) / 1e12
+    gbs = lambda b_, us: b_ / (us * 1e-6) / 1e9
+    roof = {
+        "gemm_up_gelu": {"bound": "tensor", "us": round(t_up, 2), "achieved": round(tf(ops_up, t_up), 1),
+                         "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tf(ops_up, t_up) / peak_tf, 4)},
+        "gemm_down": {"bound": "tensor", "us": round(t_down, 2), "achieved": round(tf(ops_down, t_down), 1),
+                      "peak": peak_tf, "unit": "TFLOP/s", "frac": round(tf(ops_down, t_down) / peak_tf, 4)},
+        "repack": {"bound": "hbm", "us": round(t_repack, 2), "bytes": repack_bytes,
+                   "achieved": round(gbs(repack_bytes, t_repack), 1), "peak": hbm, "unit": "GB/s",
+                   "frac": round(gbs(repack_bytes, t_repack) / hbm, 4)},
+        "pack": {"bound": "hbm", "us": round(t_pack, 2)},
+        "peak_kind": f"{peak_kind} (bf16 dense burst; HBM copy)",
+    }
+    del Qx, Qh, sh
+
+    # end to end: pinned host X in, Y back to pinned host memory, inside the events
+    Xh = torch.from_numpy(mcase.X).pin_memory()
+    Yh = torch.empty((M, N_down), dtype=torch.float32).pin_memory()
+    Xd = torch.empty_like(Xm)
+
+    def e2e_call():
+        Xd.copy_(Xh, non_blocking=True)
+        ops.convrot_mlp(Xd, G, mlp_w[0], ops.ACT_GELU, G, mlp_w[1], Y=Ym, workspace=wsm, stream=stream)
+        Yh.copy_(Ym, non_blocking=True)
+    t_e2e = timed(e2e_call, n=5)
+    e2e = {"value": round((ops_up + ops_down) / (t_e2e * 1e-6) / 1e12, 2), "unit": "TOPS", "us": round(t_e2e, 2),
+           "h2d_bytes_per_step": int(Xh.numel() * 4), "d2h_bytes_per_step": int(Yh.numel() * 4),
+           "api": "copy X host->device, convrot_mlp, copy Y device->host (pinned host buffers)"}
+    del Xh, Yh, Xd
+
+    # split SwiGLU: gate and up [12288, 3072] sharing the pack, h = silu(gate) * up
+    rng = workloads.rng_for(5)
+    Wg = torch.from_numpy(workloads.weights(rng, N_up, K)).to(dev)
+    q8, sg, qg = ops.convrot_prepare_weight(Wg, G)
+    gate = (qg, sg, torch.from_numpy(workloads.biases(rng, N_up)).to(dev), ops.convrot_weight_chunks(q8))
+    del q8, Wg
+    t_sw = timed(lambda: ops.convrot_mlp(Xm, G, (gate, mlp_w[0]), ops.ACT_SWIGLU, G, mlp_w[1], Y=Ym, workspace=wsm,
+                                         stream=stream))
+    ops_sw = 2.0 * ops_up + ops_down
+    swiglu = {"workload": f"X fp32 [{M},{K}] -> gate and up [{N_up},{K}] (one pack, one GEMM, h = silu(gate) * up "
+                          f"in its epilogue) -> repack -> down [{N_down},{N_up}], one convrot_mlp call",
+              "us": round(t_sw, 2), "TOPS": round(ops_sw / (t_sw * 1e-6) / 1e12, 2), "ops_per_call": int(ops_sw)}
+    del gate
+
+    out = {"workload": f"dit_mlp: X fp32 [{M},{K}] -> up [{N_up},{K}] + GELU (in the up GEMM's epilogue) -> "
+                       f"repack -> down [{N_down},{N_up}], G={G}, one convrot_mlp call",
+           "ms": round(t_chain * 1e-3, 4), "TOPS": round((ops_up + ops_down) / (t_chain * 1e-6) / 1e12, 2),
+           "frac": round((ops_up + ops_down) / (t_chain * 1e-6) / 1e12 / peak_tf, 4),
+           "ops_per_call": int(ops_up + ops_down),
+           "parts_us": {"pack": round(t_pack, 2), "up_gemm_gelu": round(t_up, 2), "repack": round(t_repack, 2),
+                        "down_gemm": round(t_down, 2)},
+           "gelu_placement_us": {"in_the_up_gemm_epilogue": {"up_gemm": round(t_up, 2), "repack": round(t_repack, 2)},
+                                 "in_the_repack": {"up_gemm": round(t_up_plain, 2),
+                                                   "repack": round(t_gelu_repack, 2)}},
+           "roofline": roof, "e2e": e2e, "swiglu": swiglu}
+    if with_cpu:
+        out["cpu_baseline"] = mlp_cpu_baseline(mcase, mw)
+    del Xm, mlp_w, Ym, wsm, H
+    return out
+
+
+def mlp_cpu_baseline(case, w, rows=256):
+    """The oracle MLP chain (pack, int32 GEMM, reconstruction, GELU, repack,
+    int32 GEMM, reconstruction) on the first `rows` rows, weights prepared
+    by the oracle beforehand (offline in the method, not timed)."""
+    import oracle
+    G = w.G
+    (Qu, su), (Qd, sd) = [oracle.prepare_weight(W, G) for W in case.Ws]
+    X = case.X[:rows]
+    t0 = time.perf_counter()
+    H = oracle.gelu(oracle.linear(X, Qu, su, case.bs[0], G))
+    oracle.linear(H, Qd, sd, case.bs[1], G)
+    t = time.perf_counter() - t0
+    ops_ = 2.0 * rows * (w.Ns[0] * w.K + w.Ns[1] * w.Ns[0])
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count() or 1
+    return {"value": ops_ / t / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "sample": f"oracle MLP chain on the first {rows} of {w.M} rows ({t:.2f} s; numpy/BLAS on all host cores)"}
 
 
 def small_configs_in_graph(dev, replays=5):

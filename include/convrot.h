@@ -85,7 +85,11 @@ typedef enum convrot_dtype {
 /* Activation applied to a linear's output (convrot_mlp). */
 typedef enum convrot_activation {
   CONVROT_ACT_NONE = 0,
-  CONVROT_ACT_GELU = 1 /* 0.5 y (1 + erf(y / sqrt 2)), fp32 with erff */
+  CONVROT_ACT_GELU = 1,  /* 0.5 y (1 + erf(y / sqrt 2)), fp32, erf by Abramowitz &
+                            Stegun 7.1.28 (|error| <= 3e-7) */
+  CONVROT_ACT_SWIGLU = 2 /* split SwiGLU: silu(gate) * up = (g / (1 + exp(-g))) * u
+                            of two linears sharing the input (fp32, expf and an
+                            IEEE division) */
 } convrot_activation;
 
 /* Longest activation row (K) the pack kernel holds on chip. */
@@ -308,6 +312,17 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
                                  int G, uint16_t* Q_x16, float* s_x, void* stream);
 
 /*
+ * convrot_pack_gelu_f16 -- the MLP's repack: GELU (as CONVROT_ACT_GELU)
+ * applied to every element of fp32 rows as they are loaded, then the convrot
+ * pack with the codes written as binary16 (the tensor-core GEMM's operand).
+ * GELU(X) itself is never stored.
+ *   X [M,K] fp32, Q_x16 [M,K] binary16 codes (output), s_x [M] fp32 (output).
+ * Errors: as convrot_pack_activations.
+ */
+int convrot_pack_gelu_f16(const float* X, int64_t M, int64_t K, int G, uint16_t* Q_x16, float* s_x,
+                          void* stream);
+
+/*
  * convrot_linear_packed -- the grouped GEMM of convrot_linear on an activation
  * packed by convrot_pack_activations_f16: every
  * Y_j = float(Q_x Q_wj^T) * s_x * s_wj + b_j.
@@ -322,6 +337,25 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
                           const convrot_weight* weights, int n_weights,
                           void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * convrot_linear_packed_act -- convrot_linear_packed with an activation applied
+ * in the GEMM's epilogue before the output is stored:
+ *   CONVROT_ACT_NONE    exactly convrot_linear_packed;
+ *   CONVROT_ACT_GELU    every Y_j = gelu(y_j) (as CONVROT_ACT_GELU);
+ *   CONVROT_ACT_SWIGLU  weights = {gate, up} (n_weights == 2, the same N,
+ *                       binary16 weights): weights[0].Y = silu(gate) * up
+ *                       ("ggml operator extensions", sd.cpp integration:
+ *                       split SwiGLU, the epilogue writes only the activated
+ *                       output; weights[1].Y is unused).
+ * The activation variants need N % 4 == 0. Other arguments as
+ * convrot_linear_packed.
+ * Errors: as convrot_linear_packed; ERR_UNSUPPORTED for split SwiGLU with
+ *         packed 4-bit weights.
+ */
+int convrot_linear_packed_act(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
+                              const convrot_weight* weights, int n_weights, int activation,
+                              void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * convrot_linear_host_workspace_size -- device bytes convrot_linear_host needs:
@@ -401,24 +435,50 @@ size_t convrot_mlp_workspace_size(int64_t M, int64_t K, int64_t N_up);
 /*
  * convrot_mlp -- an up linear, an activation and a down linear on the device
  * (the transformer MLP built from two convrot linears):
- *   Y_up = float(Q_x Q_up^T) * s_x * s_up + b_up       (fp32 [M, N_up]),
- *   H = act(Y_up), applied elementwise as Y_up is loaded for the pack,
+ *   Y_up = float(Q_x Q_up^T) * s_x * s_up + b_up,
+ *   H = act(Y_up), applied in the up GEMM's epilogue (fp32 [M, N_up]),
  *   Y = float(Q_h Q_down^T) * s_h * s_down + b_down  (H packed with G_down).
  *   X        [M,K] fp32/fp16 activations.
- *   up       weight of the up linear: q16 [N_up,K], scale, bias, kchunk as in
- *            convrot_linear; Y = NULL (Y_up stays in the workspace) or an fp32
- *            [M,N_up] device array that receives Y_up (before the activation).
- *   activation  CONVROT_ACT_NONE or CONVROT_ACT_GELU.
- *   down     weight of the down linear: q16 [N_down,N_up], ...; Y [M,N_down].
+ *   up       the up linear's descriptor: q16 [N_up,K] (or packed 4-bit q4),
+ *            scale, bias, kchunk as in convrot_linear; Y = NULL (H stays in
+ *            the workspace) or an fp32 [M,N_up] device array that receives H.
+ *            With CONVROT_ACT_SWIGLU, `up` points to TWO descriptors, the gate
+ *            linear then the up linear (same N_up, binary16 weights; "ggml
+ *            operator extensions", sd.cpp integration: split SwiGLU of two
+ *            GEMMs sharing the quantized input), and H = silu(gate) * up;
+ *            the first descriptor's Y receives H.
+ *   activation  CONVROT_ACT_NONE, CONVROT_ACT_GELU or CONVROT_ACT_SWIGLU.
+ *   down     weight of the down linear: q16 [N_down,N_up] (or q4), ...; Y [M,N_down].
  *   G_up / G_down  group sizes (4^n) dividing K / N_up.
  *   workspace  >= convrot_mlp_workspace_size(M, K, N_up) bytes.
  * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_WORKSPACE,
- *         ERR_UNSUPPORTED, ERR_CUDA.
+ *         ERR_UNSUPPORTED (split SwiGLU with packed 4-bit weights), ERR_CUDA.
  */
 int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int G_up,
                 const convrot_weight* up, int activation, int G_down,
                 const convrot_weight* down, void* workspace, size_t workspace_bytes,
                 void* stream);
+
+/*
+ * convrot_linear_swiglu -- split SwiGLU of two linears that share an input
+ * ("ggml operator extensions", sd.cpp integration: two INT8 GEMMs sharing a
+ * quantized input fuse with split SwiGLU, a paired-column iterator reads the
+ * separate gate and up weights, and the GEMM epilogue writes only the
+ * activated output): X is packed once, and one GEMM computes
+ *   g = float(Q_x Q_gate^T) * s_x * s_gate + b_gate,
+ *   u = float(Q_x Q_up^T) * s_x * s_up + b_up,
+ *   h = silu(g) * u = (g / (1 + exp(-g))) * u   (fp32, expf, IEEE division),
+ * writing h only.
+ *   gate_up  host array of two descriptors: the gate linear, then the up
+ *            linear; binary16 weights (q16), the same N (N % 4 == 0); h is
+ *            written to gate_up[0].Y, [M,N] fp32 (gate_up[1].Y is unused).
+ *   workspace  at least convrot_linear_workspace_size(M, K) bytes.
+ * Errors: ERR_ARG, ERR_GROUP, ERR_ALIGN, ERR_ALIAS, ERR_WORKSPACE,
+ *         ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_linear_swiglu(const void* X, int x_dtype, int64_t M, int64_t K, int G,
+                          const convrot_weight* gate_up, void* workspace, size_t workspace_bytes,
+                          void* stream);
 
 /* Size of the fixed device array that convrot_linear_noalloc uses (32 MiB). */
 #define CONVROT_NOALLOC_SCRATCH_BYTES (32u << 20)

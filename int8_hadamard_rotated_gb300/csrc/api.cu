@@ -329,11 +329,29 @@ int convrot_pack_activations_f16(const void* X, int x_dtype, int64_t M, int64_t 
   return launch_pack(X, x_dtype, M, K, G, Q_x16, kPackF16, s_x, static_cast<cudaStream_t>(stream));
 }
 
+int convrot_pack_gelu_f16(const float* X, int64_t M, int64_t K, int G, uint16_t* Q_x16, float* s_x, void* stream) {
+  if (int st = pack_checks(X, CONVROT_F32, M, K, G, Q_x16, 2, s_x)) return st;
+  if (M == 0) return CONVROT_OK;
+  return launch_pack_gelu(X, M, K, G, reinterpret_cast<__half*>(Q_x16), s_x, static_cast<cudaStream_t>(stream));
+}
+
 int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
                           const convrot_weight* weights, int n_weights,
                           void* workspace, size_t workspace_bytes, void* stream) {
+  return convrot_linear_packed_act(Q_x16, s_x, M, K, weights, n_weights, CONVROT_ACT_NONE, workspace,
+                                   workspace_bytes, stream);
+}
+
+int convrot_linear_packed_act(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
+                              const convrot_weight* weights, int n_weights, int activation,
+                              void* workspace, size_t workspace_bytes, void* stream) {
   if (M < 0 || K <= 0) return CONVROT_ERR_ARG;
+  if (activation != CONVROT_ACT_NONE && activation != CONVROT_ACT_GELU && activation != CONVROT_ACT_SWIGLU)
+    return CONVROT_ERR_ARG;
   if (int st = check_weight_list(weights, n_weights)) return st;
+  const bool swiglu = (activation == CONVROT_ACT_SWIGLU);
+  if (swiglu && (n_weights != 2 || weights[1].N != weights[0].N || weights[0].N == 0)) return CONVROT_ERR_ARG;
+  if (swiglu && (!weights[0].q16 || !weights[1].q16)) return CONVROT_ERR_UNSUPPORTED;
   if (M == 0) return CONVROT_OK;
   if (!Q_x16 || !s_x) return CONVROT_ERR_ARG;
   if (K % 16 != 0 || !aligned16(Q_x16) || !aligned16(s_x) || (workspace && !aligned16(workspace)))
@@ -344,12 +362,31 @@ int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, in
   if (workspace && (overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, Q_x16, static_cast<size_t>(M) * K * 2) ||
                     overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, s_x, static_cast<size_t>(M) * 4)))
     return CONVROT_ERR_ALIAS;
-  if (int st = check_weights(weights, n_weights, M, K, Q_x16, static_cast<size_t>(M) * K * 2, s_x,
-                             static_cast<size_t>(M) * 4))
+  // split SwiGLU: both descriptors write h to the first one's Y, so each is
+  // checked on its own, then h against the other weight's arrays
+  convrot_weight w2[2];
+  const convrot_weight* ws_list = weights;
+  if (swiglu) {
+    w2[0] = weights[0];
+    w2[1] = weights[1];
+    w2[1].Y = w2[0].Y;
+    ws_list = w2;
+    for (int j = 0; j < 2; ++j)
+      if (int st = check_weights(&w2[j], 1, M, K, Q_x16, static_cast<size_t>(M) * K * 2, s_x,
+                                 static_cast<size_t>(M) * 4))
+        return st;
+    const size_t ny = static_cast<size_t>(M) * w2[0].N * 4;
+    for (int j = 0; j < 2; ++j)
+      if (overlaps(w2[0].Y, ny, weight_codes(w2[j]), weight_code_bytes(w2[j], K)) ||
+          overlaps(w2[0].Y, ny, w2[j].scale, w2[j].N * 4) || overlaps(w2[0].Y, ny, w2[j].bias, w2[j].N * 4))
+        return CONVROT_ERR_ALIAS;
+  } else if (int st = check_weights(weights, n_weights, M, K, Q_x16, static_cast<size_t>(M) * K * 2, s_x,
+                                    static_cast<size_t>(M) * 4)) {
     return st;
+  }
   if (workspace)
     for (int j = 0; j < n_weights; ++j) {
-      const convrot_weight& w = weights[j];
+      const convrot_weight& w = ws_list[j];
       if (w.N == 0) continue;
       if (overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, w.Y, static_cast<size_t>(M) * w.N * 4) ||
           overlaps(workspace, CONVROT_GEMM_SYNC_BYTES, weight_codes(w), weight_code_bytes(w, K)) ||
@@ -358,8 +395,15 @@ int convrot_linear_packed(const uint16_t* Q_x16, const float* s_x, int64_t M, in
         return CONVROT_ERR_ALIAS;
     }
   if (int st = check_device()) return st;
-  return launch_grouped(reinterpret_cast<const __half*>(Q_x16), s_x, M, K, weights, n_weights,
-                        static_cast<cudaStream_t>(stream), 1.0f, workspace ? sync_at(workspace) : GemmSync());
+  const GemmSync sync = workspace ? sync_at(workspace) : GemmSync();
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __half* x16 = reinterpret_cast<const __half*>(Q_x16);
+  if (activation == CONVROT_ACT_NONE) return launch_grouped(x16, s_x, M, K, weights, n_weights, s, 1.0f, sync);
+  GemmLinear lins[CONVROT_MAX_LINEARS];
+  int n = 0;
+  for (int j = 0; j < n_weights; ++j)
+    if (ws_list[j].N > 0) lins[n++] = to_linear(ws_list[j], ws_list[j].Y);
+  return launch_gemm_act(x16, s_x, M, K, lins, n, activation, s, sync);
 }
 
 int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,

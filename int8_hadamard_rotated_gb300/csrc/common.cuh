@@ -368,6 +368,77 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(uint32_t M, uint32_t N) {
 }
 
 // ---------------------------------------------------------------------------
+// activations (GEMM epilogues, the MLP repack)
+// ---------------------------------------------------------------------------
+
+// GELU 0.5 y (1 + erf(y / sqrt 2)) with erf from Abramowitz & Stegun,
+// "Handbook of Mathematical Functions", formula 7.1.28 (Hastings):
+//   erf(t) = 1 - 1 / (1 + a1 t + a2 t^2 + ... + a6 t^6)^16 + e(t), |e| <= 3e-7,
+// for t >= 0. P = 1 + a1 t + ... is formed by Horner's rule in fp32, 1 / P
+// by the hardware reciprocal (rcp.approx, relative error about 2^-23) and
+// raised to the 16th power by squaring; for y < 0, 1 + erf(-t) = 1 / P^16
+// directly (no cancellation), for y >= 0, 1 + erf(t) = 2 - 1 / P^16. The
+// result stays within about 5e-7 |y| of the exact GELU. Two elements at a
+// time, on lane-wise fp32 pairs (each lane rounded as the scalar operation).
+__device__ __forceinline__ unsigned long long f32x2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f32x2_unpack(unsigned long long r, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f32x2_fma(unsigned long long a, unsigned long long b,
+                                                        unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f32x2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ float rcp_approx(float x) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+__device__ __forceinline__ void gelu_as2(float& y0, float& y1) {
+  const unsigned long long t = f32x2_mul(f32x2_pack(fabsf(y0), fabsf(y1)),
+                                         f32x2_pack(0.70710678118654752f, 0.70710678118654752f));
+  auto c = [](float v) { return f32x2_pack(v, v); };
+  unsigned long long P = f32x2_fma(t, c(0.0000430638f), c(0.0002765672f));
+  P = f32x2_fma(t, P, c(0.0001520143f));
+  P = f32x2_fma(t, P, c(0.0092705272f));
+  P = f32x2_fma(t, P, c(0.0422820123f));
+  P = f32x2_fma(t, P, c(0.0705230784f));
+  P = f32x2_fma(t, P, c(1.0f));
+  float p0, p1;
+  f32x2_unpack(P, p0, p1);
+  unsigned long long r = f32x2_pack(rcp_approx(p0), rcp_approx(p1));
+  r = f32x2_mul(r, r);  // ^2
+  r = f32x2_mul(r, r);  // ^4
+  r = f32x2_mul(r, r);  // ^8
+  r = f32x2_mul(r, r);  // ^16
+  float r0, r1;
+  f32x2_unpack(r, r0, r1);
+  const float e0 = (y0 >= 0.0f) ? 2.0f - r0 : r0;  // 1 + erf
+  const float e1 = (y1 >= 0.0f) ? 2.0f - r1 : r1;
+  f32x2_unpack(f32x2_mul(f32x2_mul(f32x2_pack(y0, y1), c(0.5f)), f32x2_pack(e0, e1)), y0, y1);
+}
+
+// silu(g) * u = g u / (1 + exp(-g)), with exp(-g) = 2^(-g log2 e) from the
+// hardware base-2 exponential (ex2.approx) and a correctly rounded
+// reciprocal: a relative error of a few 1e-7 for |g| up to ~10, the exact
+// limits 0 (g -> -inf) and g u (g -> +inf).
+__device__ __forceinline__ float silu_mul_fast(float g, float u) {
+  float e;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(-1.4426950408889634f * g));
+  return g * __frcp_rn(1.0f + e) * u;
+}
+
+// ---------------------------------------------------------------------------
 // host helpers
 // ---------------------------------------------------------------------------
 
@@ -412,8 +483,9 @@ enum PackOut { kPackI8 = 0, kPackF16 = 1 };
 int launch_pack(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                 void* out_codes, int out_kind, float* scales, cudaStream_t stream, float in_scale = 1.0f);
 
-// The same pack of fp32 rows into binary16 codes with GELU applied to every
-// element as it is loaded (the MLP's activation, fused into its repack).
+// The same pack of fp32 rows into binary16 codes with GELU (gelu_as2) applied
+// to every element as it is loaded (the MLP's activation, fused into its
+// repack).
 int launch_pack_gelu(const float* X, int64_t M, int64_t K, int G, __half* out_codes, float* scales,
                      cudaStream_t stream);
 
@@ -486,13 +558,22 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
 // unless raw_s32.
 int launch_gemm_w4(const __half* x16, const float* s_x, int64_t M, int64_t K,
                    const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
-                   GemmSync sync = GemmSync());
+                   GemmSync sync = GemmSync(), bool gelu = false);
 
 // Every linear of the list, binary16-weight and packed 4-bit ones in one
 // launch each (in that order, on the same stream and hand-over words).
 int launch_linears(const __half* x16, const float* s_x, int64_t M, int64_t K,
                    const GemmLinear* lins, int n_lin, bool raw_s32, cudaStream_t stream,
                    GemmSync sync = GemmSync());
+
+// The GEMM with an activation applied to its output before the store:
+// CONVROT_ACT_GELU (every linear), CONVROT_ACT_SWIGLU (lins[0] = gate,
+// lins[1] = up, same N; h = silu(gate) * up written to lins[0].out), or
+// CONVROT_ACT_NONE. N % 4 == 0, no input scale; packed 4-bit weights with
+// GELU or none only.
+int launch_gemm_act(const __half* x16, const float* s_x, int64_t M, int64_t K,
+                    const GemmLinear* lins, int n_lin, int act, cudaStream_t stream,
+                    GemmSync sync = GemmSync());
 
 // Activation rows per tile (256, 192 or 128) for a grouped launch (gemm.cu).
 int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool can_split);

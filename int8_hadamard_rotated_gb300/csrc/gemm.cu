@@ -58,13 +58,39 @@ namespace {
 
 using namespace gemm;
 
+constexpr int kActNone = 0;
+constexpr int kActGelu = 1;
+constexpr int kActSwiglu = 2;
+
+// K blocks per exact chunk of a tile. For split SwiGLU the tile holds the
+// features c.wt * 128 .. +127 of both weights, each one plan block: the
+// shorter of the two plans' runs.
+template <int CG, bool SWIGLU>
+__device__ __forceinline__ int chunk_kb(const GemmParams& p, const TileCoord& c) {
+  if (!SWIGLU) return tile_chunk_kb<CG>(p, c);
+  int L = KB_PER_CHUNK;
+  if (p.kchunk[0] && p.kchunk[1]) L = min(__ldg(p.kchunk[0] + c.wt), __ldg(p.kchunk[1] + c.wt));
+  return max(1, min(L, p.num_kb));
+}
+
 // UNSCALE: the variant for linears with an input scale other than 1 (the IEEE
 // division stays out of the common kernel's unrolled epilogue).
 // YTMA: Y leaves through shared memory and tensor-map stores (Y_ROWS rows x
 // 128 features per store) instead of per-thread global stores.
-template <int CG, int BN_, bool UNSCALE, bool YTMA>
+// ACT (CTA pairs with YTMA only): an activation applied to the reconstructed
+// output before it is stored.
+//   kActGelu: Y = gelu(y) elementwise.
+//   kActSwiglu: split SwiGLU of two linears that share the input, gate
+//     (linear 0) and up (linear 1) with the same N: a tile covers 128 output
+//     features, and each CTA of the pair holds 64 of them in both weights
+//     (rows 0-63 of its tile: gate, rows 64-127: up, loaded from the two
+//     weight tensors as they are). The epilogue reconstructs both and writes
+//     only h = silu(gate) * up, through a 64-feature staging tile.
+template <int CG, int BN_, bool UNSCALE, bool YTMA, int ACT = kActNone>
 __global__ void __launch_bounds__(THREADS, 1)
 convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
+  static_assert(ACT == kActNone || (CG == 2 && YTMA && !UNSCALE), "activations: pair kernel, staged stores");
+  constexpr bool SWIGLU = (ACT == kActSwiglu);
   using Gm = Geom<CG, BN_, YTMA>;
   constexpr int BN = Gm::BN;
   constexpr int COLS_PER_THREAD = Gm::COLS;
@@ -150,7 +176,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           if (CG == 2) {
             if (leader) mbar_arrive_expect_tx(&full[stage], CG * Gm::STAGE_BYTES);
             const uint32_t fb = full_leader + stage * 8u;
-            tma_load_2d_pair(sw, &p.tmap_w[c.lin], fb, kb * BK, w_row, pol_w);
+            if (SWIGLU) {
+              // this CTA's 64 features of the gate weight, then of the up weight
+              const int f = c.wt * 128 + static_cast<int>(rank) * 64;
+              tma_load_2d_pair(sw, &p.tmap_w[0], fb, kb * BK, f, pol_w);
+              tma_load_2d_pair(sw + 64 * BK * 2, &p.tmap_w[1], fb, kb * BK, f, pol_w);
+            } else {
+              tma_load_2d_pair(sw, &p.tmap_w[c.lin], fb, kb * BK, w_row, pol_w);
+            }
             tma_load_2d_pair(sx, &p.tmap_x, fb, kb * BK, x_row, pol_x);
           } else {
             mbar_arrive_expect_tx(&full[stage], Gm::STAGE_BYTES);
@@ -180,10 +213,10 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       WorkItem it, nx;
       int j = 0;
       bool have = work_item(p, unit, n_units, j, it);
-      int L = have ? tile_chunk_kb<CG>(p, decode_tile(p, it.t)) : 1;
+      int L = have ? chunk_kb<CG, SWIGLU>(p, decode_tile(p, it.t)) : 1;
       while (ok && have) {
         const bool have_nx = work_item(p, unit, n_units, ++j, nx);
-        const int L_nx = have_nx ? tile_chunk_kb<CG>(p, decode_tile(p, nx.t)) : 1;
+        const int L_nx = have_nx ? chunk_kb<CG, SWIGLU>(p, decode_tile(p, nx.t)) : 1;
         for (int c0 = it.kb0; ok && c0 < it.kb1;) {
           const int c1 = chunk_end(c0, L, it.kb1);
           const uint32_t buf = chunk_iter & 1u;
@@ -237,7 +270,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
     WorkItem it;
     for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
       const TileCoord c = decode_tile(p, it.t);
-      const int L = tile_chunk_kb<CG>(p, c);
+      const int L = chunk_kb<CG, SWIGLU>(p, c);
       // One exact chunk (the whole K of a tile that is not split) is kept as
       // the fp32 value TMEM holds: an integer below 2^24, so it is float(A)
       // itself. Several chunks, a split tile and the raw int32 output add the
@@ -284,7 +317,11 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       ok = named_bar_and(EPI_BAR, NUM_EPI_WARPS * 32, ok);
       if (!ok) break;
       const int N = p.N[c.lin];
-      const int o = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
+      // the output feature of this thread's TMEM lane (split SwiGLU: lanes
+      // 0-63 hold the gate and 64-127 the up weight of the CTA's 64 features)
+      const int o = SWIGLU ? c.wt * 128 + static_cast<int>(rank) * 64 + ((32 * quarter + lane) & 63)
+                           : c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M + 32 * quarter + lane;
+      const int wsel = (SWIGLU && 32 * quarter + lane >= 64) ? 1 : c.lin;  // the linear whose scale and bias apply
       const bool o_ok = o < N;
       const int r0 = c.xt * BN + half * COLS_PER_THREAD;
       // partial sums of a split tile travel through the tile's own output, as int32
@@ -353,8 +390,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           }
         }
         float* Y = static_cast<float*>(p.out[c.lin]);
-        const float* sw_ptr = p.s_w[c.lin];
-        const float* b_ptr = p.bias[c.lin];
+        const float* sw_ptr = p.s_w[wsel];
+        const float* b_ptr = p.bias[wsel];
         const float sw = (o_ok && sw_ptr) ? __ldg(sw_ptr + o) : 1.0f;
         const float bb = (o_ok && b_ptr) ? __ldg(b_ptr + o) : 0.0f;
         const float in_scale = UNSCALE ? p.in_scale[c.lin] : 1.0f;
@@ -373,12 +410,16 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           // before the epilogue-wide barrier of this tile
           float* ssx = reinterpret_cast<float*>(smem + Gm::SMEM_SX) + half * 128;
           if (col < COLS_PER_THREAD) ssx[col] = (r0 + col < p.M) ? __ldg(p.s_x + r0 + col) : 0.0f;
+          // (unrolled so that the accumulators stay in registers)
 #pragma unroll
           for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
             // every block commits one bulk group (empty when nothing is
             // stored) and the count of blocks per tile is even, so the group
             // two back is the last store from this buffer: wait until it read it
-            float* sy = reinterpret_cast<float*>(sy_base + (sub & 1) * Y_BUF_BYTES);
+            // (split SwiGLU: y is staged in buffer 0, reused every block, and
+            // h in one half of buffer 1 per block, the half two blocks back
+            // being the last one stored)
+            float* sy = reinterpret_cast<float*>(sy_base + (SWIGLU ? 0 : (sub & 1) * Y_BUF_BYTES));
             if (store_leader) bulk_wait_read<1>();
             named_bar_sync(1 + half, 4 * 32);
 #pragma unroll
@@ -410,16 +451,44 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
               float y0, y1, y2, y3;
               unpair_f32(ya, y0, y1);
               unpair_f32(yb, y2, y3);
+              if (ACT == kActGelu) {
+                gelu_as2(y0, y1);
+                gelu_as2(y2, y3);
+              }
               sy[i * CTA_M + col] = y0;
               sy[(i + 1) * CTA_M + col] = y1;
               sy[(i + 2) * CTA_M + col] = y2;
               sy[(i + 3) * CTA_M + col] = y3;
             }
-            fence_proxy_async_smem();
-            named_bar_sync(1 + half, 4 * 32);
-            if (store_leader) {
-              if (o_base < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
-              bulk_commit();
+            // Split SwiGLU: the product is evaluated by the warps of TMEM
+            // quarters 2 and 3 only (quarter 0 shares its scheduler with the
+            // TMA producer and quarter 1 with the MMA issuer, which pace the
+            // kernel), eight independent rows per thread.
+            const int awork = col - 64;  // 0 .. 63 in quarters 2 and 3
+            if (SWIGLU) {
+              // h = silu(gate) * up for the CTA's 64 features: gate in staged
+              // columns 0-63, up in 64-127
+              named_bar_sync(1 + half, 4 * 32);
+              float* sh = reinterpret_cast<float*>(sy_base + Y_BUF_BYTES) + (sub & 1) * (Y_ROWS * 64);
+              if (awork >= 0) {
+#pragma unroll
+                for (int i = 0; i < Y_ROWS; ++i)
+                  sh[i * 64 + awork] = silu_mul_fast(sy[i * CTA_M + awork], sy[i * CTA_M + 64 + awork]);
+              }
+              fence_proxy_async_smem();
+              named_bar_sync(1 + half, 4 * 32);
+              if (store_leader) {
+                const int f0 = c.wt * 128 + static_cast<int>(rank) * 64;
+                if (f0 < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[0], sh, f0, r0 + sub * Y_ROWS);
+                bulk_commit();
+              }
+            } else {
+              fence_proxy_async_smem();
+              named_bar_sync(1 + half, 4 * 32);
+              if (store_leader) {
+                if (o_base < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
+                bulk_commit();
+              }
             }
           }
         } else {
@@ -494,7 +563,7 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
   return CONVROT_OK;
 }
 
-template <int CG, int BN, bool UNSCALE, bool YTMA>
+template <int CG, int BN, bool UNSCALE, bool YTMA, int ACT = kActNone>
 int configure_kernel() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -503,7 +572,7 @@ int configure_kernel() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE, YTMA>,
+    e = cudaFuncSetAttribute(convrot_gemm_kernel<CG, BN, UNSCALE, YTMA, ACT>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Geom<CG, BN, YTMA>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
@@ -544,7 +613,7 @@ int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, cons
   if (p.total_tiles == 0) return CONVROT_OK;
   if (YTMA)
     for (int j = 0; j < n_lin; ++j)
-      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
+      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N, CTA_M)) return st;
   const int units = std::min(p.total_tiles, pairs);
   if (BN == 256) plan_split(p, units, 2, sync);
   cudaLaunchAttribute attr[2];
@@ -629,12 +698,12 @@ int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box
 }
 
 // fp32 Y [rows, cols] row-major (cols % 4 == 0), box 128 features x Y_ROWS rows, no swizzle.
-int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
+int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return set_cuda_error(cudaErrorNotSupported);
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 4};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(CTA_M), static_cast<cuuint32_t>(Y_ROWS)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(Y_ROWS)};
   const cuuint32_t estr[2] = {1, 1};
   CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
@@ -747,6 +816,80 @@ int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool
     if (best_cost < 0.0 || cost < best_cost) { best = bn; best_cost = cost; }
   }
   return best;
+}
+
+namespace {
+
+// The activation variants: 256-row pair tiles with staged stores. GELU takes
+// the linears as usual (and may split its last wave); split SwiGLU takes
+// lins[0] (gate) and lins[1] (up), same N, whole tiles only (a split tile's
+// partial sums of both weights would need twice the output's room), and
+// writes h to lins[0].out.
+template <int ACT>
+int launch_act(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
+               int pairs, cudaStream_t stream, const GemmSync& sync) {
+  constexpr int BN = 256;
+  GemmParams p;
+  if (ACT == kActSwiglu) {
+    if (n_lin != 2 || lins[0].N != lins[1].N) return CONVROT_ERR_ARG;
+    if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, 1, false)) return st;
+    // both weights in boxes of 64 rows; one tile per 128 features
+    if (int st = make_tmap(&p.tmap_w[0], lins[0].w16, lins[0].N, K, 64)) return st;
+    if (int st = make_tmap(&p.tmap_w[1], lins[1].w16, lins[1].N, K, 64)) return st;
+    for (int j = 0; j < 2; ++j) {
+      p.s_w[j] = lins[j].s_w;
+      p.bias[j] = lins[j].bias;
+      p.kchunk[j] = lins[j].kchunk;
+    }
+    const int wt = static_cast<int>((lins[0].N + 127) / 128);
+    p.wtile_start[0] = 0;
+    p.wtile_start[1] = wt;
+    p.n_wtiles = wt;
+    const int64_t total = static_cast<int64_t>(p.n_xtiles) * wt;
+    if (total > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+    p.total_tiles = static_cast<int>(total);
+    if (int st = make_tmap_y(&p.tmap_y[0], lins[0].out, M, lins[0].N, 64)) return st;
+  } else {
+    if (int st = fill_params<2, BN>(p, x16, s_x, M, K, lins, n_lin, false)) return st;
+    for (int j = 0; j < n_lin; ++j)
+      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N, CTA_M)) return st;
+  }
+  if (p.total_tiles == 0) return CONVROT_OK;
+  const int units = std::min(p.total_tiles, pairs);
+  if (ACT != kActSwiglu) plan_split(p, units, 2, sync);
+  if (int st = configure_kernel<2, BN, false, true, ACT>()) return st;
+  cudaLaunchAttribute attr[2];
+  const cudaLaunchConfig_t cfg = pair_config(units, Geom<2, BN, true>::SMEM_ALLOC, stream, attr, true);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_kernel<2, BN, false, true, ACT>, p);
+  if (e != cudaSuccess) return set_cuda_error(e);
+  return check_launch();
+}
+
+}  // namespace
+
+int launch_gemm_act(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
+                    int act, cudaStream_t stream, GemmSync sync) {
+  if (M == 0) return CONVROT_OK;
+  if (act == CONVROT_ACT_NONE) return launch_linears(x16, s_x, M, K, lins, n_lin, false, stream, sync);
+  bool w4 = false;
+  for (int j = 0; j < n_lin; ++j) {
+    if (lins[j].N % 4 != 0) return CONVROT_ERR_ALIGN;
+    if (lins[j].in_scale != 1.0f) return CONVROT_ERR_UNSUPPORTED;
+    w4 |= !lins[j].w16;
+  }
+  if (w4) {
+    // packed 4-bit weights: GELU in the S8 x S4 GEMM's epilogue (every linear W4)
+    if (act != CONVROT_ACT_GELU) return CONVROT_ERR_UNSUPPORTED;
+    for (int j = 0; j < n_lin; ++j)
+      if (lins[j].w16) return CONVROT_ERR_UNSUPPORTED;
+    return launch_gemm_w4(x16, s_x, M, K, lins, n_lin, false, stream, sync, true);
+  }
+  if (int st = configure_kernel<2, 256, false, true>()) return st;
+  const int pairs = max_pairs<256>();
+  if (pairs <= 0) return CONVROT_ERR_UNSUPPORTED;
+  if (act == CONVROT_ACT_GELU) return launch_act<kActGelu>(x16, s_x, M, K, lins, n_lin, pairs, stream, sync);
+  if (act == CONVROT_ACT_SWIGLU) return launch_act<kActSwiglu>(x16, s_x, M, K, lins, n_lin, pairs, stream, sync);
+  return CONVROT_ERR_ARG;
 }
 
 int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,

@@ -231,8 +231,8 @@ __device__ __forceinline__ int tile_chunk_kb(const GemmParams& p, const TileCoor
 
 // fp16 [rows, K] row-major tensor map, box box_rows x 64, 128-byte swizzle.
 int make_tmap(CUtensorMap* m, const void* base, int64_t rows, int64_t K, int box_rows);
-// fp32 Y [rows, cols] row-major (cols % 4 == 0), box 128 features x Y_ROWS rows.
-int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols);
+// fp32 Y [rows, cols] row-major (cols % 4 == 0), box box_cols features x Y_ROWS rows.
+int make_tmap_y(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_cols = CTA_M);
 // Nonzero value distinct per launch for the hand-over flags.
 unsigned long long next_epoch();
 // Whether splitting the fractional last wave of T tiles over `units` pays.

@@ -149,7 +149,9 @@ __device__ __forceinline__ void widen_w4x8(uint32_t w, uint32_t (&h)[4]) {
   }
 }
 
-template <int BN_, bool UNSCALE>
+// GELU: the output is gelu(y) (gelu_as2: the Abramowitz & Stegun 7.1.28 erf;
+// the MLP's activation applied where the up linear's output is stored).
+template <int BN_, bool UNSCALE, bool GELU = false>
 __global__ void __launch_bounds__(W4_THREADS, 1)
 convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
   using Gm = GeomW4<BN_>;
@@ -485,6 +487,10 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
             float y0, y1, y2, y3;
             unpair_f32(ya, y0, y1);
             unpair_f32(yb, y2, y3);
+            if (GELU) {
+              gelu_as2(y0, y1);
+              gelu_as2(y2, y3);
+            }
             sy[i * CTA_M + col] = y0;
             sy[(i + 1) * CTA_M + col] = y1;
             sy[(i + 2) * CTA_M + col] = y2;
@@ -547,7 +553,7 @@ int fill_params_w4(GemmParams& p, const __half* x16, const float* s_x, int64_t M
   for (int j = 0; j < n_lin; ++j) {
     if (int st = make_tmap_w4(&p.tmap_w[j], lins[j].w4, lins[j].N, K)) return st;
     if (!raw_s32)
-      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N)) return st;
+      if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N, CTA_M)) return st;
     p.s_w[j] = lins[j].s_w;
     p.bias[j] = lins[j].bias;
     p.kchunk[j] = nullptr;
@@ -574,7 +580,7 @@ int fill_params_w4(GemmParams& p, const __half* x16, const float* s_x, int64_t M
   return CONVROT_OK;
 }
 
-template <int BN, bool UNSCALE>
+template <int BN, bool UNSCALE, bool GELU = false>
 int configure_w4() {
   static std::mutex mu;
   static uint64_t configured = 0;  // bit d: attribute set on device d
@@ -583,7 +589,7 @@ int configure_w4() {
   if (e != cudaSuccess) return set_cuda_error(e);
   std::lock_guard<std::mutex> lock(mu);
   if (dev >= 64 || !((configured >> dev) & 1u)) {
-    e = cudaFuncSetAttribute(convrot_gemm_w4_kernel<BN, UNSCALE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(convrot_gemm_w4_kernel<BN, UNSCALE, GELU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              GeomW4<BN>::SMEM_ALLOC);
     if (e != cudaSuccess) return set_cuda_error(e);
     if (dev < 64) configured |= (1ull << dev);
@@ -615,7 +621,7 @@ int max_pairs_w4() {
   return cached[dev];
 }
 
-template <int BN, bool UNSCALE>
+template <int BN, bool UNSCALE, bool GELU = false>
 int launch_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
               bool raw_s32, int pairs, cudaStream_t stream, const GemmSync& sync) {
   GemmParams p;
@@ -623,11 +629,11 @@ int launch_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, const G
   if (p.total_tiles == 0) return CONVROT_OK;
   const int units = std::min(p.total_tiles, pairs);
   if (BN == 256) plan_split(p, units, 2, sync);
-  if (int st = configure_w4<BN, UNSCALE>()) return st;
+  if (int st = configure_w4<BN, UNSCALE, GELU>()) return st;
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = pair_config(units, GeomW4<BN>::SMEM_ALLOC, stream, attr, true);
   cfg.blockDim = dim3(W4_THREADS, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_w4_kernel<BN, UNSCALE>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, convrot_gemm_w4_kernel<BN, UNSCALE, GELU>, p);
   if (e != cudaSuccess) return set_cuda_error(e);
   return check_launch();
 }
@@ -635,7 +641,7 @@ int launch_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, const G
 }  // namespace
 
 int launch_gemm_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, const GemmLinear* lins, int n_lin,
-                   bool raw_s32, cudaStream_t stream, GemmSync sync) {
+                   bool raw_s32, cudaStream_t stream, GemmSync sync, bool gelu) {
   if (M == 0) return CONVROT_OK;
   if (K % 64 != 0 || K > CONVROT_W4_MAX_K) return CONVROT_ERR_UNSUPPORTED;
   bool unscale = false;
@@ -644,6 +650,7 @@ int launch_gemm_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, co
     if (!raw_s32 && lins[j].N % 4 != 0) return CONVROT_ERR_ALIGN;  // Y rows of whole 16-byte units
   }
   if (raw_s32 && unscale) return CONVROT_ERR_ARG;
+  if (gelu && (raw_s32 || unscale)) return CONVROT_ERR_ARG;
   if (int st = configure_w4<256, false>()) return st;
   if (int st = configure_w4<192, false>()) return st;
   if (int st = configure_w4<128, false>()) return st;
@@ -651,6 +658,11 @@ int launch_gemm_w4(const __half* x16, const float* s_x, int64_t M, int64_t K, co
   if (pairs <= 0) return CONVROT_ERR_UNSUPPORTED;
   const bool can_split = sync.words && sync.bytes >= static_cast<size_t>(2 * pairs) * sizeof(unsigned long long);
   const int bn = pick_tile_rows(M, lins, n_lin, pairs, can_split);
+  if (gelu) {
+    if (bn == 128) return launch_w4<128, false, true>(x16, s_x, M, K, lins, n_lin, false, pairs, stream, sync);
+    if (bn == 192) return launch_w4<192, false, true>(x16, s_x, M, K, lins, n_lin, false, pairs, stream, sync);
+    return launch_w4<256, false, true>(x16, s_x, M, K, lins, n_lin, false, pairs, stream, sync);
+  }
   if (unscale) {
     if (bn == 128) return launch_w4<128, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);
     if (bn == 192) return launch_w4<192, true>(x16, s_x, M, K, lins, n_lin, raw_s32, pairs, stream, sync);

@@ -53,11 +53,11 @@
 //   pack_kernel (any K % 16 == 0, rows up to 32768 elements): per-thread
 //     16-byte cp.async copies into a lane-interleaved two-stage buffer and
 //     direct 16-byte stores of the codes.
-// An elementwise prologue may transform each loaded row first: GELU, or the
-// modulation (RMS norm, per-channel weight, (x + x*scale) + shift). The
-// modulated pack takes pack_tma_kernel for rows of up to kVecSmemMaxK
-// features, with the three modulation vectors staged once per CTA in shared
-// memory, and pack_kernel for longer rows.
+// A prologue may transform each loaded row first: GELU, or the modulation
+// (RMS norm, per-channel weight, (x + x*scale) + shift). The modulated pack takes
+// pack_tma_kernel for rows of up to kVecSmemMaxK features, with the three
+// modulation vectors staged once per CTA in shared memory, and pack_kernel
+// for longer rows.
 #include "common.cuh"
 
 #include <algorithm>
@@ -433,9 +433,10 @@ __device__ __forceinline__ void scale_unit(float (&v)[16], float a) {
   for (int p = 0; p < 16; ++p) v[p] = __fmul_rn(v[p], a);
 }
 
-// Elementwise prologue applied to the loaded row before everything else:
-// none, or GELU 0.5 x (1 + erf(x / sqrt 2)) in fp32 with CUDA's erff (the MLP
-// activation, applied where its output is quantized for the down linear).
+// Prologue applied to the loaded rows before the rotation: none, GELU (the
+// MLP's activation, gelu_as2, applied where its output is quantized for the
+// down linear), or the modulation (per-row RMS norm, per-channel weight,
+// (x + x*scale) + shift).
 constexpr int kProNone = 0;
 constexpr int kProGelu = 1;
 constexpr int kProModulate = 2;  // per-row RMS norm and per-channel weight / modulation (ModPrologue)
@@ -444,8 +445,7 @@ template <int PRO>
 __device__ __forceinline__ void prologue_unit(float (&v)[16]) {
   if (PRO == kProGelu) {
 #pragma unroll
-    for (int p = 0; p < 16; ++p)
-      v[p] = __fmul_rn(__fmul_rn(0.5f, v[p]), __fadd_rn(1.0f, erff(__fmul_rn(v[p], 0.70710678118654752f))));
+    for (int p = 0; p < 16; p += 2) gelu_as2(v[p], v[p + 1]);
   }
 }
 

@@ -34,6 +34,7 @@ ERR_SCRATCH = 11
 
 ACT_NONE = 0
 ACT_GELU = 1
+ACT_SWIGLU = 2
 
 F32 = 0
 F16 = 1
@@ -93,6 +94,9 @@ SIGNATURES = {
     "convrot_w4_expand": (_I, [_VP, _I64, _I64, _VP, _VP, _VP]),
     "convrot_pack_activations_f16": (_I, [_VP, _I, _I64, _I64, _I, _VP, _VP, _VP]),
     "convrot_linear_packed": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP, _SZ, _VP]),
+    "convrot_pack_gelu_f16": (_I, [_VP, _I64, _I64, _I, _VP, _VP, _VP]),
+    "convrot_linear_packed_act": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _I, _VP, _SZ,
+                                       _VP]),
     "convrot_linear_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64]),
     "convrot_linear_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I64, _VP, _SZ,
                                  _VP, _VP, _VP]),
@@ -100,6 +104,7 @@ SIGNATURES = {
     "convrot_mlp": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I,
                          ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
+    "convrot_linear_swiglu": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_device_status": (_I, [_VP]),
 }
 
@@ -416,6 +421,40 @@ def convrot_linear_packed(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, 
     return Ys
 
 
+def convrot_linear_packed_act(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases, activation: int,
+                              Ys=None, stream=None, kchunks=None, workspace=None):
+    """convrot_linear_packed with an activation in the GEMM's epilogue: GELU
+    on every output, or split SwiGLU of q16s = [gate, up] (returns [h])."""
+    _need(Q_x16, torch.float16, "Q_x16")
+    _need(s_x, torch.float32, "s_x")
+    M, K = Q_x16.shape
+    if Ys is None:
+        n_out = 1 if activation == ACT_SWIGLU else len(q16s)
+        Ys = [torch.empty((M, q16s[j].shape[0]), dtype=torch.float32, device=Q_x16.device) for j in range(n_out)]
+    outs = [Ys[0], Ys[0]] if activation == ACT_SWIGLU else Ys
+    weights = make_weights(q16s, scales, biases, outs, kchunks)
+    ws = _workspace(GEMM_SYNC_BYTES, Q_x16.device, workspace)
+    _check(lib().convrot_linear_packed_act(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), activation, _ptr(ws),
+                                           ws.numel() * ws.element_size(), _stream(stream)),
+           "convrot_linear_packed_act")
+    return Ys
+
+
+def convrot_pack_gelu_f16(X: torch.Tensor, G: int, Q_x16: Optional[torch.Tensor] = None,
+                          s_x: Optional[torch.Tensor] = None, stream=None):
+    """The MLP's repack: GELU applied to fp32 X as it is loaded, then the pack
+    into binary16 codes and row scales."""
+    _need(X, torch.float32, "X")
+    M, K = X.shape
+    if Q_x16 is None:
+        Q_x16 = torch.empty((M, K), dtype=torch.float16, device=X.device)
+    if s_x is None:
+        s_x = torch.empty((M,), dtype=torch.float32, device=X.device)
+    _check(lib().convrot_pack_gelu_f16(_ptr(X), M, K, G, _ptr(Q_x16), _ptr(s_x), _stream(stream)),
+           "convrot_pack_gelu_f16")
+    return Q_x16, s_x
+
+
 def convrot_linear_host_workspace_size(M: int, K: int, x_dtype: int, n_total: int, chunk_rows: int = 0) -> int:
     return int(lib().convrot_linear_host_workspace_size(M, K, x_dtype, n_total, chunk_rows))
 
@@ -458,19 +497,22 @@ def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: 
                 stream=None) -> torch.Tensor:
     """Up linear, activation, down linear on the device. `up` and `down` are
     (weight codes, scale, bias, kchunk) tuples, the codes binary16 [N, K] or
-    packed 4-bit [N, K/2] (uint8); H (optional, fp32 [M, N_up]) receives the
-    up linear's output before the activation."""
+    packed 4-bit [N, K/2] (uint8); with ACT_SWIGLU `up` is a pair of such
+    tuples, (gate, up). H (optional, fp32 [M, N_up]) receives the activated
+    up output that the down linear packs (GELU(Y_up), or with ACT_SWIGLU
+    h = silu(gate) * up)."""
     xd = _xdtype(X)
     _need(X, X.dtype, "X")
     M, K = X.shape
-    uq, us, ub, uk = up
+    ups = list(up) if activation == ACT_SWIGLU else [up]
     dq, ds, db, dk = down
-    N_up, N_down = uq.shape[0], dq.shape[0]
+    N_up, N_down = ups[0][0].shape[0], dq.shape[0]
     if Y is None:
         Y = torch.empty((M, N_down), dtype=torch.float32, device=X.device)
     if H is not None:
         _need(H, torch.float32, "H")
-    wu = make_weights([uq], [us], [ub], [H], [uk])
+    wu = make_weights([u[0] for u in ups], [u[1] for u in ups], [u[2] for u in ups], [H] * len(ups),
+                      [u[3] for u in ups])
     wd = make_weights([dq], [ds], [db], [Y], [dk])
     ws = _workspace(convrot_mlp_workspace_size(M, K, N_up), X.device, workspace)
     _check(lib().convrot_mlp(_ptr(X), xd, M, K, G_up, wu, activation, G_down, wd, _ptr(ws), ws.numel(),
@@ -501,3 +543,23 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
 
 def convrot_device_status(stream=None) -> int:
     return int(lib().convrot_device_status(_stream(stream)))
+
+
+def convrot_linear_swiglu(X: torch.Tensor, G: int, gate: Tuple, up: Tuple, H: Optional[torch.Tensor] = None,
+                          workspace=None, stream=None) -> torch.Tensor:
+    """Split SwiGLU of two linears sharing X: h = silu(gate) * up, where gate
+    and up are (q16, scale, bias, kchunk) tuples with the same N; one pack and
+    one GEMM whose epilogue writes only h (fp32 [M, N])."""
+    xd = _xdtype(X)
+    _need(X, X.dtype, "X")
+    M, K = X.shape
+    N = gate[0].shape[0]
+    if H is None:
+        H = torch.empty((M, N), dtype=torch.float32, device=X.device)
+    _need(H, torch.float32, "H")
+    w = make_weights([gate[0], up[0]], [gate[1], up[1]], [gate[2], up[2]], [H, H], [gate[3], up[3]])
+    ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
+    _check(lib().convrot_linear_swiglu(_ptr(X), xd, M, K, G, w, _ptr(ws), ws.numel(), _stream(stream)),
+           "convrot_linear_swiglu")
+    return H
+

@@ -27,6 +27,9 @@ Readings where the pages leave a step open (each listed in the design notes):
   * An all-zero row has s = 0 and Q = 0.
   * Y is rounded to fp32 after every operation: ((float(A) * s_x) * s_w) + b.
   * The MLP pair's GELU is the exact-erf GELU, formed in fp64, rounded to fp32.
+  * Split SwiGLU is h = silu(gate) * up with silu(g) = g / (1 + exp(-g)),
+    gate and up each the output of a convrot linear, formed in fp64 from
+    their fp32 values and rounded once to fp32.
 
 Every function is pinned in tests/test_oracle_pins.py against facts the pages
 or mathematics fix (the printed H4, orthogonality, closed forms, brute force).
@@ -52,6 +55,8 @@ __all__ = [
     "prologue",
     "unpack_w4",
     "gelu",
+    "silu_mul",
+    "linear_swiglu",
 ]
 
 # "INT8 Convrot Safetensors" -- How INT8 convrot works: the regular Hadamard
@@ -265,3 +270,24 @@ def gelu(Y: np.ndarray) -> np.ndarray:
     from scipy.special import erf  # library erf, fp64
     y = np.asarray(Y, dtype=np.float64)
     return (0.5 * y * (1.0 + erf(y / math.sqrt(2.0)))).astype(np.float32)
+
+
+def silu_mul(gate: np.ndarray, up: np.ndarray) -> np.ndarray:
+    """Split SwiGLU: h = silu(gate) * up, silu(g) = g / (1 + exp(-g)), formed in
+    fp64 from the fp32 inputs and rounded once to fp32. ("ggml operator
+    extensions", sd.cpp integration: two INT8 GEMMs sharing a quantized input
+    fuse with split SwiGLU; the gate and up weights stay separate.)"""
+    g = np.asarray(gate, dtype=np.float32).astype(np.float64)
+    u = np.asarray(up, dtype=np.float32).astype(np.float64)
+    with np.errstate(over="ignore"):
+        sg = g / (1.0 + np.exp(-g))
+    return (sg * u).astype(np.float32)
+
+
+def linear_swiglu(X: np.ndarray, Qg: np.ndarray, s_g, b_g, Qu: np.ndarray, s_u, b_u, G: int) -> np.ndarray:
+    """The split-SwiGLU pair on one packed input: h = silu(gate) * up, gate and
+    up each the convrot linear of X (the same pack) with its own weight."""
+    Qx, s_x = pack(X, G)
+    gate = reconstruct(gemm_s32(Qx, Qg), s_x, s_g, b_g)
+    up = reconstruct(gemm_s32(Qx, Qu), s_x, s_u, b_u)
+    return silu_mul(gate, up)

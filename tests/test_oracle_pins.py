@@ -617,3 +617,65 @@ def test_unpack_w4_pins():
     back = ((q[:, 0::2] & 0xF) | ((q[:, 1::2] & 0xF) << 4)).astype(np.uint8)
     np.testing.assert_array_equal(back, allb)
     assert q.min() == -8 and q.max() == 7
+
+
+def check_silu_mul(mod=orc):
+    """silu(g) * u against facts of the logistic function: silu(0) = 0;
+    silu(1) = e / (1 + e) and silu(-1) = -1 / (1 + e); silu(g) - silu(-g) = g;
+    silu(g) = g (1 + tanh(g / 2)) / 2; silu saturates to g for large g and to
+    0 for very negative g; the gate is the silu argument, the up input only
+    scales it."""
+    import math
+    f32 = np.float32
+    e = math.e
+    one = np.ones(5, f32)
+    g = np.array([0.0, 1.0, -1.0, 40.0, -200.0], f32)
+    h = mod.silu_mul(g, one).astype(np.float64)
+    expect = [0.0, e / (1 + e), -1 / (1 + e), 40.0, 0.0]
+    np.testing.assert_allclose(h, np.array(expect, f32), rtol=1e-7, atol=1e-30)
+    x = np.linspace(-6, 6, 49).astype(f32)
+    d = mod.silu_mul(x, np.ones_like(x)).astype(np.float64) - mod.silu_mul(-x, np.ones_like(x)).astype(np.float64)
+    np.testing.assert_allclose(d, x.astype(np.float64), rtol=1e-6, atol=1e-6)
+    th = x.astype(np.float64) * (1 + np.tanh(x.astype(np.float64) / 2)) / 2
+    np.testing.assert_allclose(mod.silu_mul(x, np.ones_like(x)), th.astype(f32), rtol=1e-6, atol=1e-7)
+    # the up input scales the result linearly; the gate is not symmetric with it
+    u = np.full_like(x, 3.0)
+    np.testing.assert_allclose(mod.silu_mul(x, u), 3.0 * mod.silu_mul(x, np.ones_like(x)), rtol=1e-6, atol=1e-6)
+    assert mod.silu_mul(np.array([2.0], f32), np.array([-1.0], f32))[0] != \
+        mod.silu_mul(np.array([-1.0], f32), np.array([2.0], f32))[0]
+
+
+def test_silu_mul_pins():
+    check_silu_mul()
+
+
+def _silu_swapped(gate, up):
+    return orc.silu_mul(up, gate)
+
+
+def _sigmoid_only(gate, up):
+    g = np.asarray(gate, np.float64)
+    return (np.asarray(up, np.float64) / (1.0 + np.exp(-g))).astype(np.float32)
+
+
+@pytest.mark.parametrize("bad", [_silu_swapped, _sigmoid_only], ids=["gate-up-swapped", "sigmoid-not-silu"])
+def test_planted_silu_mistakes_are_caught(bad):
+    assert _fails(_Mutant(silu_mul=bad), (check_silu_mul,))
+
+
+def test_linear_swiglu_is_the_two_linears():
+    """linear_swiglu is silu_mul of the two convrot linears on the same pack."""
+    rng = np.random.default_rng(8)
+    M, K, N, G = 12, 256, 40, 64
+    X = rng.standard_normal((M, K)).astype(np.float32)
+    Wg = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    Wu = (rng.standard_normal((N, K)) * 0.05).astype(np.float32)
+    Qg, sg = oracle.prepare_weight(Wg, G)
+    Qu, su = oracle.prepare_weight(Wu, G)
+    h = oracle.linear_swiglu(X, Qg, sg, None, Qu, su, None, G)
+    np.testing.assert_array_equal(h, oracle.silu_mul(oracle.linear(X, Qg, sg, None, G), oracle.linear(X, Qu, su, None, G)))
+    # and it approximates silu(X Wg^T) * (X Wu^T) within the quantization error
+    ref = X.astype(np.float64) @ Wg.T.astype(np.float64)
+    ref = ref / (1 + np.exp(-ref)) * (X.astype(np.float64) @ Wu.T.astype(np.float64))
+    assert np.max(np.abs(h - ref)) <= 0.05 * np.max(np.abs(ref))
+
