@@ -511,6 +511,26 @@ int convrot_linear_noalloc(const void* X, int x_dtype, int64_t M, int64_t K, int
                            void* stream);
 
 /*
+ * convrot_test_handover_timeout -- a test of the GEMM's timeout path, not part
+ * of the method: convrot_linear_packed (binary16 weights, the hand-over words
+ * in `workspace`) with every bounded device wait of the launch limited to
+ * wait_ns nanoseconds, and the CTA pairs that finish split tiles waiting for a
+ * hand-over value that no pair publishes. On a shape whose last wave is split
+ * (e.g. M = 4608 with three 3072 x 3072 linears), those waits give up: the
+ * kernel records CONVROT_ERR_TIMEOUT in the device's error word, skips its
+ * remaining work, waits (bounded) for its copies in flight, releases its tensor
+ * memory and exits; the outputs are incomplete. convrot_device_status then
+ * returns CONVROT_ERR_TIMEOUT and clears the word; the device, the stream and
+ * the workspace stay usable (the next launch publishes new hand-over values).
+ * Nothing traps or hangs.
+ * Errors: ERR_ARG (also wait_ns == 0 or packed 4-bit weights), ERR_ALIGN,
+ *         ERR_WORKSPACE, ERR_OVERFLOW, ERR_ALIAS, ERR_UNSUPPORTED, ERR_CUDA.
+ */
+int convrot_test_handover_timeout(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
+                                  const convrot_weight* weights, int n_weights, void* workspace,
+                                  size_t workspace_bytes, uint64_t wait_ns, void* stream);
+
+/*
  * convrot_device_status -- synchronizes `stream`, then returns and clears the
  * device's sticky error word: CONVROT_OK, or CONVROT_ERR_TIMEOUT when a
  * kernel's bounded wait on a TMA or tensor-core completion barrier gave up

@@ -406,6 +406,29 @@ int convrot_linear_packed_act(const uint16_t* Q_x16, const float* s_x, int64_t M
   return launch_gemm_act(x16, s_x, M, K, lins, n, activation, s, sync);
 }
 
+int convrot_test_handover_timeout(const uint16_t* Q_x16, const float* s_x, int64_t M, int64_t K,
+                                  const convrot_weight* weights, int n_weights, void* workspace,
+                                  size_t workspace_bytes, uint64_t wait_ns, void* stream) {
+  if (M <= 0 || K <= 0 || wait_ns == 0) return CONVROT_ERR_ARG;
+  if (int st = check_weight_list(weights, n_weights)) return st;
+  for (int j = 0; j < n_weights; ++j)
+    if (weights[j].q4) return CONVROT_ERR_ARG;  // the binary16-weight GEMM
+  if (!Q_x16 || !s_x || !workspace) return CONVROT_ERR_ARG;
+  if (K % 16 != 0 || !aligned16(Q_x16) || !aligned16(s_x) || !aligned16(workspace)) return CONVROT_ERR_ALIGN;
+  if (workspace_bytes < CONVROT_GEMM_SYNC_BYTES) return CONVROT_ERR_WORKSPACE;
+  if (K > CONVROT_MAX_K) return CONVROT_ERR_OVERFLOW;
+  if (M > 0x7fffffff) return CONVROT_ERR_UNSUPPORTED;
+  if (int st = check_weights(weights, n_weights, M, K, Q_x16, static_cast<size_t>(M) * K * 2, s_x,
+                             static_cast<size_t>(M) * 4))
+    return st;
+  if (int st = check_device()) return st;
+  GemmSync sync = sync_at(workspace);
+  sync.test_wait_ns = wait_ns;
+  sync.test_unpublished_handover = true;
+  return launch_grouped(reinterpret_cast<const __half*>(Q_x16), s_x, M, K, weights, n_weights,
+                        static_cast<cudaStream_t>(stream), 1.0f, sync);
+}
+
 int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                    const convrot_weight* weights, int n_weights,
                    void* workspace, size_t workspace_bytes, void* stream) {

@@ -76,17 +76,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait until the phase with the given parity has completed. Returns false
 // (after recording a timeout in *err_word) if it does not complete within
-// kWaitLimitNs, or early if `*abort_flag` (shared; may be null) is set by
+// limit_ns, or early if `*abort_flag` (shared; may be null) is set by
 // another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          volatile int* abort_flag, int* err_word) {
+                                          volatile int* abort_flag, int* err_word,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63) == 63) {
       if (abort_flag && *abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         if (abort_flag) *abort_flag = 1;
         record_error(err_word, CONVROT_ERR_TIMEOUT);
         return false;
@@ -541,6 +542,11 @@ int launch_chunk_plan(const int8_t* Q_w, int64_t N, int64_t K, int32_t* kchunk, 
 struct GemmSync {
   unsigned long long* words = nullptr;
   size_t bytes = 0;
+  // test of the timeout path (convrot_test_handover_timeout): a wait limit for
+  // the launch (0: the normal kWaitLimitNs) and whether the tails of split
+  // tiles wait for a hand-over value that no head publishes
+  unsigned long long test_wait_ns = 0;
+  bool test_unpublished_handover = false;
 };
 
 // The hand-over words at `base` (CONVROT_GEMM_SYNC_BYTES of workspace).

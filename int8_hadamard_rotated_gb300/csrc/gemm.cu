@@ -170,7 +170,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         const int w_row = c.wt * Gm::TILE_M + static_cast<int>(rank) * CTA_M;
         const int x_row = c.xt * BN + static_cast<int>(rank) * Gm::X_ROWS;
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
           uint8_t* sw = smem + stage * Gm::STAGE_BYTES;
           uint8_t* sx = sw + Gm::W_BYTES;
           if (CG == 2) {
@@ -201,7 +201,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         for (uint32_t s = 0; s < STAGES; ++s)
           if (n_issued > s) {
             const uint32_t uses = (n_issued - 1 - s) / STAGES + 1;  // times stage s was filled
-            mbar_wait(&full[s], (uses - 1) & 1u, nullptr, err);
+            mbar_wait(&full[s], (uses - 1) & 1u, nullptr, err, p.wait_ns);
           }
     }
     __syncwarp();
@@ -221,14 +221,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           const int c1 = chunk_end(c0, L, it.kb1);
           const uint32_t buf = chunk_iter & 1u;
           const uint32_t use = chunk_iter >> 1;
-          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + buf * BN;
           const int kb0 = c0;
           const int kb1 = c1;
           c0 = c1;
           for (int kb = kb0; kb < kb1; ++kb) {
-            if (!mbar_wait(&full[stage], phase, abort_flag, err)) { ok = false; break; }
+            if (!mbar_wait(&full[stage], phase, abort_flag, err, p.wait_ns)) { ok = false; break; }
             tc_fence_after();
             const uint32_t sw = smem_u32(smem + stage * Gm::STAGE_BYTES);
             const uint64_t a_desc = smem_desc_sw128(sw);
@@ -254,7 +254,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       }
       // all issued MMAs complete before TMEM is released
       if (CG == 2) mma_commit_pair(drain, static_cast<uint16_t>(1u << lead_rank)); else mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, err);
+      mbar_wait(drain, 0, nullptr, err, p.wait_ns);
     }
     __syncwarp();
   } else {
@@ -283,7 +283,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
       for (int c0 = it.kb0; c0 < it.kb1; c0 = chunk_end(c0, L, it.kb1)) {
         const uint32_t buf = chunk_iter & 1u;
         const uint32_t use = chunk_iter >> 1;
-        if (!mbar_wait(&tfull[buf], use & 1u, abort_flag, err)) { ok = false; break; }
+        if (!mbar_wait(&tfull[buf], use & 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
         tc_fence_after();
         if (int_path) {
 #pragma unroll
@@ -343,7 +343,7 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
         bool got = true;
         if (threadIdx.x == 0) {
           unsigned long long* f = p.sk_flags + UNIT_CTAS * (unit - 1) + crank;
-          got = wait_flag(f, p.epoch, abort_flag, err);
+          got = wait_flag(f, p.epoch ^ p.handover_xor, abort_flag, err, p.wait_ns);
           if (got) st_relaxed_gpu(f, 0ull);  // consumed: zero again for the next launch
         }
         ok = named_bar_and(EPI_BAR, NUM_EPI_WARPS * 32, got);
@@ -560,6 +560,8 @@ int fill_params(GemmParams& p, const __half* x16, const float* s_x, int64_t M, i
   p.n_lin = n_lin;
   p.raw_s32 = raw_s32 ? 1 : 0;
   p.sk_tiles = 0;
+  p.wait_ns = kWaitLimitNs;
+  p.handover_xor = 0;
   return CONVROT_OK;
 }
 
@@ -616,6 +618,8 @@ int launch_pairs(const __half* x16, const float* s_x, int64_t M, int64_t K, cons
       if (int st = make_tmap_y(&p.tmap_y[j], lins[j].out, M, lins[j].N, CTA_M)) return st;
   const int units = std::min(p.total_tiles, pairs);
   if (BN == 256) plan_split(p, units, 2, sync);
+  if (sync.test_wait_ns) p.wait_ns = sync.test_wait_ns;
+  if (sync.test_unpublished_handover) p.handover_xor = 1;
   cudaLaunchAttribute attr[2];
   const cudaLaunchConfig_t cfg = pair_config(units, Geom<2, BN, YTMA>::SMEM_ALLOC, stream, attr, true);
   if (int st = configure_kernel<2, BN, UNSCALE, YTMA>()) return st;

@@ -93,6 +93,12 @@ struct GemmParams {
   int sk_tiles;
   unsigned long long* sk_flags;    // [2 * units]: one word per CTA of a pair
   unsigned long long epoch;        // nonzero, distinct per launch
+  // Bounded waits: every wait of the launch gives up after wait_ns
+  // (kWaitLimitNs normally). A test of the timeout path shortens it and sets
+  // handover_xor, so that the tails of split tiles wait for epoch ^ handover_xor,
+  // a value no head publishes (0 normally).
+  unsigned long long wait_ns;
+  unsigned long long handover_xor;
 };
 
 struct TileCoord {
@@ -172,13 +178,13 @@ __device__ __forceinline__ int chunk_end(int c0, int L, int kb1) {
 // Bounded wait until *flag == v (acquire). On giving up: sets the CTA's abort
 // flag, records CONVROT_ERR_TIMEOUT and returns false.
 __device__ __forceinline__ bool wait_flag(const unsigned long long* flag, unsigned long long v,
-                                          volatile int* abort_flag, int* err) {
+                                          volatile int* abort_flag, int* err, uint64_t limit_ns = kWaitLimitNs) {
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 0;; ++it) {
     if (ld_acquire_gpu(flag) == v) return true;
     if ((it & 15) == 15) {
       if (*abort_flag) return false;
-      if (global_timer_ns() - t0 > kWaitLimitNs) {
+      if (global_timer_ns() - t0 > limit_ns) {
         *abort_flag = 1;
         record_error(err, CONVROT_ERR_TIMEOUT);
         return false;

@@ -235,13 +235,13 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
             // the slot is free once the MMAs of block n - XS have finished
             if (n >= slots) {
               const uint32_t m = n - slots;
-              if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+              if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
             }
             if (leader) mbar_arrive_expect_tx(&x_full[s], 2 * Gm::X_BYTES);
             tma_load_2d_pair(smem + Gm::SMEM_X + s * Gm::X_BYTES, &p.tmap_x, x_full_leader + s * 8u, kb * BK,
                              x_row, pol);
           } else {
-            if (!mbar_wait(&pk_empty[s], ph ^ 1u, abort_flag, err)) { ok = false; break; }
+            if (!mbar_wait(&pk_empty[s], ph ^ 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
             mbar_arrive_expect_tx(&pk_full[s], PW_BYTES);
             tma_load_2d(smem + Gm::SMEM_PW + s * PW_BYTES, &p.tmap_w[c.lin], &pk_full[s], kb * (BK / 2), w_row,
                         pol);
@@ -254,8 +254,8 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       for (uint32_t t = 0; t < slots; ++t)
         if (n > t) {
           const uint32_t tph = ((n - 1 - t) / slots) & 1u;
-          if (!is_x) mbar_wait(&pk_full[t], tph, nullptr, err);
-          else if (leader) mbar_wait(&x_full[t], tph, nullptr, err);
+          if (!is_x) mbar_wait(&pk_full[t], tph, nullptr, err, p.wait_ns);
+          else if (leader) mbar_wait(&x_full[t], tph, nullptr, err, p.wait_ns);
         }
     }
     __syncwarp();
@@ -270,12 +270,12 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       for (int j = 0; ok && work_item(p, unit, n_units, j, it); ++j) {
         const uint32_t buf = acc_iter & 1u;
         const uint32_t use = acc_iter >> 1;
-        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err)) break;
+        if (!mbar_wait(&tempty[buf], (use & 1u) ^ 1u, abort_flag, err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + buf * BN;
         for (int kb = it.kb0; kb < it.kb1; ++kb) {
-          if (!mbar_wait(&x_full[xs], xph, abort_flag, err)) { ok = false; break; }
-          if (!mbar_wait(&w_full[ws], wph, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait(&x_full[xs], xph, abort_flag, err, p.wait_ns)) { ok = false; break; }
+          if (!mbar_wait(&w_full[ws], wph, abort_flag, err, p.wait_ns)) { ok = false; break; }
           tc_fence_after();
           // descriptors advance by the slot offset (address >> 4 in the low field)
           const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(ws * (Gm::W_BYTES >> 4));
@@ -296,7 +296,7 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       }
       // all issued MMAs complete before TMEM is released
       mma_commit_pair(drain, 0x1u);
-      mbar_wait(drain, 0, nullptr, err);
+      mbar_wait(drain, 0, nullptr, err, p.wait_ns);
     }
     __syncwarp();
   } else if (conv_slot(warp)) {
@@ -321,7 +321,7 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       for (int kb = it.kb0; kb < it.kb1; ++kb, ++n) {
         if ((n & (CONV_PAIRS - 1)) != q) continue;
         const uint32_t ps = n & (PK_SLOTS - 1), ws = n % W_SLOTS;
-        if (!mbar_wait(&pk_full[ps], (n / PK_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+        if (!mbar_wait(&pk_full[ps], (n / PK_SLOTS) & 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
         // widen into registers first (off the weight slot's critical path),
         // hand the packed slot back, then store once the weight slot is free
         constexpr int NCH = PW_BYTES / (2 * 32 * 16);  // 16-byte chunks per lane
@@ -341,7 +341,7 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
         // the weight slot is free once the MMAs of block n - W_SLOTS have finished
         if (n >= static_cast<uint32_t>(W_SLOTS)) {
           const uint32_t m = n - W_SLOTS;
-          if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err)) { ok = false; break; }
+          if (!mbar_wait(&done[m & (DONE_SLOTS - 1)], (m / DONE_SLOTS) & 1u, abort_flag, err, p.wait_ns)) { ok = false; break; }
         }
         uint8_t* sw = smem + Gm::SMEM_W + ws * Gm::W_BYTES;
 #pragma unroll
@@ -384,13 +384,13 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       if (it.kind == kTail) {
         if (threadIdx.x == 0) {
           unsigned long long* f = p.sk_flags + 2 * (unit - 1) + rank;
-          ok = wait_flag(f, p.epoch, abort_flag, err);
+          ok = wait_flag(f, p.epoch ^ p.handover_xor, abort_flag, err, p.wait_ns);
           if (ok) st_relaxed_gpu(f, 0ull);  // consumed: zero again for the next launch
         }
       }
       const uint32_t buf = acc_iter & 1u;
       const uint32_t use = acc_iter >> 1;
-      if (ok) ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, err);
+      if (ok) ok = mbar_wait(&tfull[buf], use & 1u, abort_flag, err, p.wait_ns);
       // the eight epilogue warps agree before any barrier of the stores below
       if (!named_bar_and(EPI_BAR, NUM_EPI_WARPS * 32, ok)) break;
       tc_fence_after();
@@ -577,6 +577,8 @@ int fill_params_w4(GemmParams& p, const __half* x16, const float* s_x, int64_t M
   p.total_tiles = static_cast<int>(total);
   p.n_lin = n_lin;
   p.raw_s32 = raw_s32 ? 1 : 0;
+  p.wait_ns = kWaitLimitNs;
+  p.handover_xor = 0;
   return CONVROT_OK;
 }
 

@@ -106,6 +106,8 @@ SIGNATURES = {
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
     "convrot_linear_swiglu": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_device_status": (_I, [_VP]),
+    "convrot_test_handover_timeout": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP, _SZ,
+                                           ctypes.c_uint64, _VP]),
 }
 
 
@@ -543,6 +545,25 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
 
 def convrot_device_status(stream=None) -> int:
     return int(lib().convrot_device_status(_stream(stream)))
+
+
+def convrot_test_handover_timeout(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases, wait_ns: int,
+                                  workspace: torch.Tensor, Ys=None, stream=None):
+    """Test-only GEMM launch whose split-tile hand-over waits can never be
+    satisfied and give up after wait_ns: the kernel records CONVROT_ERR_TIMEOUT
+    (read it with convrot_device_status) and exits, leaving those tiles of Ys
+    unfinished. Returns Ys."""
+    _need(Q_x16, torch.float16, "Q_x16")
+    _need(s_x, torch.float32, "s_x")
+    M, K = Q_x16.shape
+    if Ys is None:
+        Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=Q_x16.device) for q in q16s]
+    weights = make_weights(q16s, scales, biases, Ys)
+    _check(lib().convrot_test_handover_timeout(_ptr(Q_x16), _ptr(s_x), M, K, weights, len(q16s), _ptr(workspace),
+                                               workspace.numel() * workspace.element_size(), int(wait_ns),
+                                               _stream(stream)),
+           "convrot_test_handover_timeout")
+    return Ys
 
 
 def convrot_linear_swiglu(X: torch.Tensor, G: int, gate: Tuple, up: Tuple, H: Optional[torch.Tensor] = None,

@@ -204,3 +204,17 @@ def test_w4_descriptor_checks(L):
     assert g(A0, 16, 256, A1, 64, A2, A3, 100, None) == ops.ERR_WORKSPACE
     assert g(A0, 16, 256, A1, 64, A1 + 64, A3, big, None) == ops.ERR_ALIAS
     assert g(A0, 0, 256, A1, 64, A2, A3, big, None) == ops.OK
+
+
+def test_timeout_test_entry_checks(L):
+    """The timeout-path test entry point checks its arguments like the GEMM."""
+    from int8_hadamard_rotated_gb300 import ops
+    W = ops.convrot_weight
+    wts = (W * 1)(W(A1, A2, A3, 64, A4, None))
+    f = L.convrot_test_handover_timeout
+    sync = ops.GEMM_SYNC_BYTES
+    assert f(A0, A5, 16, 256, wts, 1, A6, sync, 0, None) == ops.ERR_ARG          # no wait limit
+    assert f(A0, A5, 16, 256, wts, 1, None, 0, 1000, None) == ops.ERR_ARG        # hand-over words required
+    assert f(A0, A5, 16, 256, wts, 1, A6, sync - 8, 1000, None) == ops.ERR_WORKSPACE
+    w4 = (W * 1)(W(None, A2, A3, 64, A4, None, A1))
+    assert f(A0, A5, 16, 256, w4, 1, A6, sync, 1000, None) == ops.ERR_ARG        # binary16 weights only
