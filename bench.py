@@ -814,7 +814,7 @@ def next_rows_legs(X, w, dev, flush, hbm, q16s, scales, biases, plans, ops_step,
     t_lin = timed(lambda: ops.convrot_linear(X, w.G, q16s, scales, biases, Ys=Ys, workspace=ws, stream=stream,
                                              weights=wdesc))
     t_scaled = timed(lambda: ops.convrot_linear_scaled(X, w.G, 0.37, q16s, scales, biases, Ys=Ys, workspace=ws,
-                                                       stream=stream, kchunks=plans))
+                                                       stream=stream, weights=wdesc))
     f4 = {"workload": f"{w.name}: one convrot_linear_scaled call, input scale 0.37", "bound": "tensor",
           "us": round(t_scaled, 2), "TOPS": round(ops_step / (t_scaled * 1e-6) / 1e12, 2),
           "plain_linear_us": round(t_lin, 2), "plain_linear_TOPS": round(ops_step / (t_lin * 1e-6) / 1e12, 2)}

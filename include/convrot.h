@@ -531,6 +531,26 @@ int convrot_test_handover_timeout(const uint16_t* Q_x16, const float* s_x, int64
                                   size_t workspace_bytes, uint64_t wait_ns, void* stream);
 
 /*
+ * convrot_test_unscale_sweep -- a test of the GEMM epilogue's unscaling step,
+ * not part of the method. The epilogue divides by a linear's input scale a
+ * without a division per element (Markstein's correction step: r = RN(1/a),
+ * q0 = RN(y r), RN(q0 + (y - q0 a) r) with the remainder exact in one FMA),
+ * which equals the IEEE quotient while a, y and the quotient stay in the
+ * normal range (a in [2^-20, 2^20], nonzero |y| in [2^-100, 2^100]; the
+ * epilogue takes the IEEE division elsewhere). This call runs that step, on
+ * the GPU, for each divisor divisors[i] (device, fp32, 16-byte aligned) and
+ * every one of the 2^23 values y = 1.m * 2^y_exp, against the IEEE division.
+ *   mismatches  device uint64, 8-byte aligned: the count of results that
+ *               differ in any bit is added to it.
+ *   first       device uint64: lowered (atomic min) to (i << 32 | bits of y)
+ *               of the smallest differing pair; set it to ~0 beforehand.
+ *   n_divisors  1 .. 65535;  y_exp  -98 .. 97.
+ * Asynchronous on `stream`. Errors: ERR_ARG, ERR_ALIGN, ERR_CUDA.
+ */
+int convrot_test_unscale_sweep(const float* divisors, int n_divisors, int y_exp, uint64_t* mismatches,
+                               uint64_t* first, void* stream);
+
+/*
  * convrot_device_status -- synchronizes `stream`, then returns and clears the
  * device's sticky error word: CONVROT_OK, or CONVROT_ERR_TIMEOUT when a
  * kernel's bounded wait on a TMA or tensor-core completion barrier gave up

@@ -429,6 +429,18 @@ int convrot_test_handover_timeout(const uint16_t* Q_x16, const float* s_x, int64
                         static_cast<cudaStream_t>(stream), 1.0f, sync);
 }
 
+int convrot_test_unscale_sweep(const float* divisors, int n_divisors, int y_exp, uint64_t* mismatches,
+                               uint64_t* first, void* stream) {
+  if (!divisors || !mismatches || !first || n_divisors < 1 || n_divisors > 65535) return CONVROT_ERR_ARG;
+  if (y_exp < -98 || y_exp > 97) return CONVROT_ERR_ARG;  // inside the step's range
+  if (!aligned16(divisors) || reinterpret_cast<uintptr_t>(mismatches) % 8 != 0 ||
+      reinterpret_cast<uintptr_t>(first) % 8 != 0)
+    return CONVROT_ERR_ALIGN;
+  if (int st = check_device()) return st;
+  return launch_unscale_sweep(divisors, n_divisors, y_exp, reinterpret_cast<unsigned long long*>(mismatches),
+                              reinterpret_cast<unsigned long long*>(first), static_cast<cudaStream_t>(stream));
+}
+
 int convrot_linear(const void* X, int x_dtype, int64_t M, int64_t K, int G,
                    const convrot_weight* weights, int n_weights,
                    void* workspace, size_t workspace_bytes, void* stream) {

@@ -581,6 +581,13 @@ int launch_gemm_act(const __half* x16, const float* s_x, int64_t M, int64_t K,
                     const GemmLinear* lins, int n_lin, int act, cudaStream_t stream,
                     GemmSync sync = GemmSync());
 
+// Test of the GEMM epilogue's unscaling step (gemm.cu): for each of
+// n_divisors divisors a and every significand of y = 1.m * 2^y_exp, the step
+// against the IEEE division; adds the count of results that differ to
+// *mismatches and lowers *first to the smallest (index << 32 | y bits) of them.
+int launch_unscale_sweep(const float* divisors, int n_divisors, int y_exp, unsigned long long* mismatches,
+                         unsigned long long* first, cudaStream_t stream);
+
 // Activation rows per tile (256, 192 or 128) for a grouped launch (gemm.cu).
 int pick_tile_rows(int64_t M, const GemmLinear* lins, int n_lin, int pairs, bool can_split);
 

@@ -410,6 +410,21 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
           // before the epilogue-wide barrier of this tile
           float* ssx = reinterpret_cast<float*>(smem + Gm::SMEM_SX) + half * 128;
           if (col < COLS_PER_THREAD) ssx[col] = (r0 + col < p.M) ? __ldg(p.s_x + r0 + col) : 0.0f;
+          // unscaling: the tile's extreme row scales decide, per thread,
+          // whether the correction step may replace the division
+          Unscale us{};
+          bool us_fast = false;
+          if (UNSCALE) {
+            named_bar_sync(1 + half, 4 * 32);
+            float v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) v[k] = (lane + 32 * k < COLS_PER_THREAD) ? ssx[lane + 32 * k] : 0.0f;
+            float lo, hi;
+            warp_scale_range(v, lo, hi);
+            us = make_unscale(in_scale);
+            us_fast = unscale_fast_ok(in_scale, lo, hi, sw);
+          }
+          const unsigned long long m1 = pair_f32(-1.0f, -1.0f);
           // (unrolled so that the accumulators stay in registers)
 #pragma unroll
           for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
@@ -436,17 +451,31 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
                 ya = mul_f32x2(ya, sw2);
                 yb = mul_f32x2(yb, sw2);
               }
-              if (UNSCALE) {
-                // unscale before the bias (IEEE division, element by element)
-                float a0, a1, a2, a3;
-                unpair_f32(ya, a0, a1);
-                unpair_f32(yb, a2, a3);
-                ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
-                yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
-              }
-              if (b_ptr) {
-                ya = add_f32x2(ya, bb2);
-                yb = add_f32x2(yb, bb2);
+              if (UNSCALE && us_fast) {
+                // unscale before the bias: -RN(y / a) by the correction step,
+                // then RN(b - (-q)) or -(-q)
+                ya = neg_unscale_f32x2(ya, us);
+                yb = neg_unscale_f32x2(yb, us);
+                if (b_ptr) {
+                  ya = f32x2_fma(ya, m1, bb2);
+                  yb = f32x2_fma(yb, m1, bb2);
+                } else {
+                  ya = mul_f32x2(ya, m1);
+                  yb = mul_f32x2(yb, m1);
+                }
+              } else {
+                if (UNSCALE) {
+                  // unscale before the bias (IEEE division, element by element)
+                  float a0, a1, a2, a3;
+                  unpair_f32(ya, a0, a1);
+                  unpair_f32(yb, a2, a3);
+                  ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
+                  yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
+                }
+                if (b_ptr) {
+                  ya = add_f32x2(ya, bb2);
+                  yb = add_f32x2(yb, bb2);
+                }
               }
               float y0, y1, y2, y3;
               unpair_f32(ya, y0, y1);
@@ -492,6 +521,14 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             }
           }
         } else {
+          Unscale us{};
+          bool us_fast = false;
+          if (UNSCALE) {
+            float lo, hi;
+            warp_scale_range(sxv, lo, hi);
+            us = make_unscale(in_scale);
+            us_fast = unscale_fast_ok(in_scale, lo, hi, sw);
+          }
 #pragma unroll
           for (int i = 0; i < COLS_PER_THREAD; ++i) {
             const float sx = __shfl_sync(0xffffffffu, sxv[i >> 5], i & 31);
@@ -500,7 +537,8 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
               // float(A) * s_x * s_w + b, one rounding per operation, in that order
               float y = __fmul_rn(__int_as_float(acc[i]), sx);
               if (sw_ptr) y = __fmul_rn(y, sw);
-              if (UNSCALE) y = __fdiv_rn(y, in_scale);  // unscale before the bias
+              // unscale before the bias
+              if (UNSCALE) y = us_fast ? -neg_unscale_f32(y, us) : __fdiv_rn(y, in_scale);
               if (b_ptr) y = __fadd_rn(y, bb);
               st_global_hint(Y + static_cast<int64_t>(r) * N + o, y, pol_y);
             }
@@ -941,6 +979,52 @@ int launch_gemm(const __half* x16, const float* s_x, int64_t M, int64_t K,
     if (int st = configure_kernel<1, 256, false, false>()) return st;
     convrot_gemm_kernel<1, 256, false, false><<<grid, THREADS, Geom<1, 256>::SMEM_ALLOC, stream>>>(p);
   }
+  return check_launch();
+}
+
+namespace {
+
+// The epilogue's unscaling step (neg_unscale_f32x2) against the IEEE division
+// for one divisor per blockIdx.y and every significand of y = 1.m * 2^y_exp,
+// two at a time; counts the results that differ in any bit and keeps the
+// smallest (divisor index, y bits) of those.
+constexpr int SWEEP_THREADS = 256;
+constexpr int SWEEP_PER_THREAD = 16;  // significands per thread, in pairs
+__global__ void __launch_bounds__(SWEEP_THREADS) unscale_sweep_kernel(const float* __restrict__ divisors,
+                                                                      int y_exp, unsigned long long* mismatches,
+                                                                      unsigned long long* first) {
+  const float a = divisors[blockIdx.y];
+  const Unscale u = make_unscale(a);
+  const uint32_t e_bits = static_cast<uint32_t>(y_exp + 127) << 23;
+  const uint32_t m0 = (blockIdx.x * SWEEP_THREADS + threadIdx.x) * SWEEP_PER_THREAD;
+  unsigned n_bad = 0;
+  unsigned long long worst = ~0ull;
+#pragma unroll
+  for (int i = 0; i < SWEEP_PER_THREAD; i += 2) {
+    const float y0 = __uint_as_float(e_bits | (m0 + i)), y1 = __uint_as_float(e_bits | (m0 + i + 1));
+    float n0, n1;
+    unpair_f32(neg_unscale_f32x2(pair_f32(y0, y1), u), n0, n1);
+    const bool bad0 = __float_as_uint(-n0) != __float_as_uint(__fdiv_rn(y0, a));
+    const bool bad1 = __float_as_uint(-n1) != __float_as_uint(__fdiv_rn(y1, a));
+    const unsigned long long tag = static_cast<unsigned long long>(blockIdx.y) << 32;
+    if (bad0) worst = min(worst, tag | __float_as_uint(y0));
+    if (bad1) worst = min(worst, tag | __float_as_uint(y1));
+    n_bad += bad0 + bad1;
+  }
+  if (n_bad) {
+    atomicAdd(mismatches, static_cast<unsigned long long>(n_bad));
+    atomicMin(first, worst);
+  }
+}
+
+}  // namespace
+
+int launch_unscale_sweep(const float* divisors, int n_divisors, int y_exp, unsigned long long* mismatches,
+                         unsigned long long* first, cudaStream_t stream) {
+  constexpr int per_block = SWEEP_THREADS * SWEEP_PER_THREAD;
+  static_assert((1 << 23) % per_block == 0, "whole blocks of significands");
+  const dim3 grid((1 << 23) / per_block, n_divisors);
+  unscale_sweep_kernel<<<grid, SWEEP_THREADS, 0, stream>>>(divisors, y_exp, mismatches, first);
   return check_launch();
 }
 

@@ -169,6 +169,74 @@ __device__ __forceinline__ unsigned long long add_f32x2(unsigned long long a, un
   return r;
 }
 
+// Unscaling by a linear's input scale a (y / a, correctly rounded) without a
+// division per element: Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Develop. 34(1), 1990; the division theorem of his
+// "IA-64 and Elementary Functions", 2000). With r = RN(1/a) and
+// q0 = RN(y r), which lies within one ulp of y / a, the remainder y - q0 a
+// is a floating-point number that one FMA returns exactly, and
+// RN(q0 + (y - q0 a) r) = RN(y / a). The argument holds while a, y, the
+// quotient and the remainder stay in the normal range: a in [2^-20, 2^20]
+// and every nonzero |y| in [2^-100, 2^100] (y = +0 gives +0 as the
+// division does). The epilogue checks that per thread and tile from the
+// extreme row scales and takes the IEEE division otherwise.
+constexpr float kUnscaleDivisorLo = 0x1p-20f, kUnscaleDivisorHi = 0x1p20f;
+// Bounds on RN(s_x s_w) that keep every nonzero y = RN(RN(float(A) s_x) s_w),
+// 1 <= |A| <= 2^31, inside [2^-98, 2^98].
+constexpr float kUnscaleScaleLo = 0x1p-98f, kUnscaleScaleHi = 0x1p67f;
+
+struct Unscale {
+  unsigned long long a2, nr2;  // (a, a) and (-RN(1/a), -RN(1/a))
+  float a, nr;
+};
+
+__device__ __forceinline__ Unscale make_unscale(float a) {
+  Unscale u;
+  u.a = a;
+  u.nr = -__frcp_rn(a);
+  u.a2 = pair_f32(a, a);
+  u.nr2 = pair_f32(u.nr, u.nr);
+  return u;
+}
+
+// Whether the correction step is exact for every y of a tile whose nonzero row
+// scales lie in [sx_lo, sx_hi], at weight scale sw (NaN and inf fail).
+__device__ __forceinline__ bool unscale_fast_ok(float a, float sx_lo, float sx_hi, float sw) {
+  const float m = fabsf(a);
+  return m >= kUnscaleDivisorLo && m <= kUnscaleDivisorHi && __fmul_rn(sx_lo, sw) >= kUnscaleScaleLo &&
+         __fmul_rn(sx_hi, sw) <= kUnscaleScaleHi;
+}
+
+// -RN(y / a) for both lanes of y2 (the negated form saves the negations:
+// RN is symmetric, so -q0 = RN(y (-r)) and -RN(q0 + rem r) = RN(rem (-r) - q0)).
+__device__ __forceinline__ unsigned long long neg_unscale_f32x2(unsigned long long y2, const Unscale& u) {
+  const unsigned long long nq0 = mul_f32x2(y2, u.nr2);  // -q0
+  const unsigned long long rem = f32x2_fma(nq0, u.a2, y2);  // y - q0 a, exact
+  return f32x2_fma(rem, u.nr2, nq0);
+}
+__device__ __forceinline__ float neg_unscale_f32(float y, const Unscale& u) {
+  const float nq0 = __fmul_rn(y, u.nr);
+  const float rem = __fmaf_rn(nq0, u.a, y);
+  return __fmaf_rn(rem, u.nr, nq0);
+}
+
+// The smallest nonzero and the largest of 32 lanes' nonnegative fp32 values
+// v[0..n) (as bit patterns, which order like the values; no nonzero value
+// gives +inf as the smallest).
+template <int NV>
+__device__ __forceinline__ void warp_scale_range(const float (&v)[NV], float& lo, float& hi) {
+  unsigned l = 0x7f800000u, h = 0u;
+#pragma unroll
+  for (int k = 0; k < NV; ++k) {
+    const unsigned b = __float_as_uint(v[k]);
+    l = min(l, b ? b : 0x7f800000u);
+    h = max(h, b);
+  }
+  lo = __uint_as_float(__reduce_min_sync(0xffffffffu, l));
+  hi = __uint_as_float(__reduce_max_sync(0xffffffffu, h));
+}
+
 // End of the exact chunk that starts at K block c0 (chunks are aligned runs of
 // L blocks inside a tile), clipped to kb1.
 __device__ __forceinline__ int chunk_end(int c0, int L, int kb1) {

@@ -407,6 +407,21 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
       float* ssx = reinterpret_cast<float*>(smem + Gm::SMEM_SX) + half * 128;
       const bool staged = !p.raw_s32 && it.kind != kHead;
       if (staged && col < COLS) ssx[col] = (r0 + col < p.M) ? __ldg(p.s_x + r0 + col) : 0.0f;
+      // unscaling: the tile's extreme row scales decide, per thread, whether
+      // the correction step may replace the division
+      Unscale us{};
+      bool us_fast = false;
+      if (UNSCALE && staged) {
+        named_bar_sync(1 + half, 4 * 32);
+        float v[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = (lane + 32 * k < COLS) ? ssx[lane + 32 * k] : 0.0f;
+        float lo, hi;
+        warp_scale_range(v, lo, hi);
+        us = make_unscale(in_scale);
+        us_fast = unscale_fast_ok(in_scale, lo, hi, sw);
+      }
+      const unsigned long long m1 = pair_f32(-1.0f, -1.0f);
 #pragma unroll 1
       for (int q = 0; q < COLS / 32; ++q) {
         uint32_t acc[32];
@@ -473,16 +488,29 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
               ya = mul_f32x2(ya, sw2);
               yb = mul_f32x2(yb, sw2);
             }
-            if (UNSCALE) {
-              float a0, a1, a2, a3;
-              unpair_f32(ya, a0, a1);
-              unpair_f32(yb, a2, a3);
-              ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
-              yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
-            }
-            if (b_ptr) {
-              ya = add_f32x2(ya, bb2);
-              yb = add_f32x2(yb, bb2);
+            if (UNSCALE && us_fast) {
+              // -RN(y / a) by the correction step, then RN(b - (-q)) or -(-q)
+              ya = neg_unscale_f32x2(ya, us);
+              yb = neg_unscale_f32x2(yb, us);
+              if (b_ptr) {
+                ya = f32x2_fma(ya, m1, bb2);
+                yb = f32x2_fma(yb, m1, bb2);
+              } else {
+                ya = mul_f32x2(ya, m1);
+                yb = mul_f32x2(yb, m1);
+              }
+            } else {
+              if (UNSCALE) {
+                float a0, a1, a2, a3;
+                unpair_f32(ya, a0, a1);
+                unpair_f32(yb, a2, a3);
+                ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
+                yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
+              }
+              if (b_ptr) {
+                ya = add_f32x2(ya, bb2);
+                yb = add_f32x2(yb, bb2);
+              }
             }
             float y0, y1, y2, y3;
             unpair_f32(ya, y0, y1);

@@ -11,6 +11,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import struct
 from typing import List, Optional, Sequence, Tuple
 
 import torch
@@ -108,6 +109,7 @@ SIGNATURES = {
     "convrot_device_status": (_I, [_VP]),
     "convrot_test_handover_timeout": (_I, [_VP, _VP, _I64, _I64, ctypes.POINTER(convrot_weight), _I, _VP, _SZ,
                                            ctypes.c_uint64, _VP]),
+    "convrot_test_unscale_sweep": (_I, [_VP, _I, _I, _VP, _VP, _VP]),
 }
 
 
@@ -328,7 +330,7 @@ def convrot_linear(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor],
 def convrot_linear_scaled(X: torch.Tensor, G: int, input_scale: float, q16s: Sequence[torch.Tensor],
                           scales: Sequence[Optional[torch.Tensor]], biases: Sequence[Optional[torch.Tensor]],
                           Ys: Optional[List[torch.Tensor]] = None, workspace=None, stream=None,
-                          kchunks=None) -> List[torch.Tensor]:
+                          kchunks=None, weights=None) -> List[torch.Tensor]:
     """convrot_linear with an input scale: X is scaled before the pack and
     every output unscaled before its bias."""
     xd = _xdtype(X)
@@ -337,7 +339,8 @@ def convrot_linear_scaled(X: torch.Tensor, G: int, input_scale: float, q16s: Seq
     if Ys is None:
         Ys = [torch.empty((M, q.shape[0]), dtype=torch.float32, device=X.device) for q in q16s]
     ws = _workspace(convrot_linear_workspace_size(M, K), X.device, workspace)
-    weights = make_weights(q16s, scales, biases, Ys, kchunks)
+    if weights is None:
+        weights = make_weights(q16s, scales, biases, Ys, kchunks)
     _check(lib().convrot_linear_scaled(_ptr(X), xd, M, K, G, float(input_scale), weights, len(q16s), _ptr(ws),
                                        ws.numel(), _stream(stream)), "convrot_linear_scaled")
     return Ys
@@ -545,6 +548,25 @@ def convrot_linear_noalloc(X: torch.Tensor, G: int, q16s: Sequence[torch.Tensor]
 
 def convrot_device_status(stream=None) -> int:
     return int(lib().convrot_device_status(_stream(stream)))
+
+
+def convrot_test_unscale_sweep(divisors: torch.Tensor, y_exp: int, stream=None) -> Tuple[int, Optional[Tuple[float, float]]]:
+    """Test-only: the GEMM epilogue's unscaling step against the IEEE division
+    for every divisor in `divisors` (fp32, on the device) and all 2^23 values
+    y = 1.m * 2^y_exp. Returns (count of results that differ, (divisor, y) of
+    the first of them or None)."""
+    _need(divisors, torch.float32, "divisors")
+    out = torch.tensor([0, -1], dtype=torch.int64, device=divisors.device)  # count, first (~0)
+    _check(lib().convrot_test_unscale_sweep(_ptr(divisors), divisors.numel(), int(y_exp), _ptr(out),
+                                            out.data_ptr() + 8, _stream(stream)),
+           "convrot_test_unscale_sweep")
+    n, first = (int(v) for v in out.cpu())
+    if n == 0:
+        return 0, None
+    first &= (1 << 64) - 1
+    d = float(divisors[first >> 32].item())
+    y = struct.unpack("<f", struct.pack("<I", first & 0xffffffff))[0]
+    return n, (d, y)
 
 
 def convrot_test_handover_timeout(Q_x16: torch.Tensor, s_x: torch.Tensor, q16s, scales, biases, wait_ns: int,

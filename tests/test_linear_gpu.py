@@ -206,3 +206,65 @@ def test_input_scale_epilogue_bit_exact(ops):
         ref = ref / a + case.bs[j][None, :]
         np.testing.assert_array_equal(host(Ys[j]), ref)
     assert ops.convrot_device_status() == ops.OK
+
+
+def _sweep_divisors():
+    """Divisors for the unscaling sweep: every significand pattern class that
+    matters to a reciprocal (1, just above 1, just below 2, all ones, thirds,
+    tenths), the scales the tests use, and seeded random significands, at
+    exponents across the step's range [2^-20, 2^20]."""
+    rng = np.random.default_rng(20241)
+    sig = [1.0, 1.0 + 2.0 ** -23, 1.0 + 2.0 ** -22, 2.0 - 2.0 ** -23, 2.0 - 2.0 ** -22, 1.5, 1.25, 1.75,
+           4.0 / 3.0, 5.0 / 3.0, 1.1, 1.2, 1.3, 1.4, 1.6, 1.7, 1.8, 1.9, 0.37 * 4, 0.5 * 3]
+    sig = [float(np.float32(v)) for v in sig]
+    sig += list(1.0 + rng.integers(0, 1 << 23, size=4096 - len(sig)) * 2.0 ** -23)
+    exps = rng.integers(-20, 20, size=len(sig))
+    exps[:len(exps) // 8] = 0
+    d = np.ldexp(np.asarray(sig, np.float64), exps).astype(np.float32)
+    return d
+
+
+@pytest.mark.parametrize("y_exp", [0, -98, 97])
+def test_unscale_step_equals_ieee_division(ops, y_exp):
+    """The epilogue's division by the input scale (Markstein's correction step
+    after a correctly rounded reciprocal) against the GPU's IEEE division, for
+    4096 divisors and all 2^23 significands of y each (the step's results scale
+    exactly with the exponents of y and a inside its range, so the significands
+    at the range ends and in the middle cover it)."""
+    d = torch.from_numpy(_sweep_divisors()).cuda()
+    n, first = ops.convrot_test_unscale_sweep(d, y_exp)
+    assert n == 0, f"{n} results differ, the first at divisor {first[0]!r}, y {first[1]!r}"
+
+
+@pytest.mark.parametrize("a", [np.float32(0.37), np.float32(1.0 / 3.0), np.float32(2.0 - 2.0 ** -22),
+                               np.float32(1.0e-7), np.float32(3.0e6)])
+def test_input_scale_epilogue_bit_exact_scales(ops, a):
+    """The scaled linear on the DiT projections equals, bit for bit, the
+    host's fp32 reconstruction ((float(A) * s_x) * s_w) / a + b with the
+    IEEE division, for divisors inside the correction step's range and
+    outside it (1e-7 and 3e6 take the division), with rows of tiny
+    activations (row scales near 1e-36, whose tiles take the division) mixed
+    in."""
+    w = workloads.get("dit_qkv")
+    case = workloads.make_case(w, M=1000)
+    X = case.X.copy()
+    X[17] *= np.float32(1e-38)
+    X[600:603] *= np.float32(1e-35)
+    M, K, G = X.shape[0], w.K, w.G
+    preps = [ops.convrot_prepare_weight(dev(W), G) for W in case.Ws]
+    q16s, scales = [p[2] for p in preps], [p[1] for p in preps]
+    biases = [dev(case.bs[0]), None, dev(case.bs[2])]
+    ws = torch.empty((ops.convrot_linear_workspace_size(M, K),), dtype=torch.uint8, device="cuda")
+    Ys = ops.convrot_linear_scaled(dev(X), G, float(a), q16s, scales, biases, workspace=ws)
+    Q8 = ws[: M * K * 2].view(torch.float16).view(M, K).to(torch.int8)
+    off = (M * K * 2 + 255) // 256 * 256
+    s_x = host(ws[off: off + 4 * M].view(torch.float32))
+    assert s_x[17] < 1e-30 * s_x[0] and s_x[601] < 1e-27 * s_x[0]
+    for j in range(3):
+        A = host(ops.int8_gemm_s32(Q8, Q_w16=q16s[j]))
+        ref = (A.astype(np.float32) * s_x[:, None]) * host(scales[j])[None, :]
+        ref = ref / a
+        if biases[j] is not None:
+            ref = ref + case.bs[j][None, :]
+        np.testing.assert_array_equal(host(Ys[j]).view(np.uint32), ref.astype(np.float32).view(np.uint32))
+    assert ops.convrot_device_status() == ops.OK
