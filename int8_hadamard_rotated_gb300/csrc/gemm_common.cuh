@@ -215,6 +215,14 @@ __device__ __forceinline__ unsigned long long neg_unscale_f32x2(unsigned long lo
   const unsigned long long rem = f32x2_fma(nq0, u.a2, y2);  // y - q0 a, exact
   return f32x2_fma(rem, u.nr2, nq0);
 }
+// The IEEE division of both lanes by a, out of line: the fallback of tiles
+// outside the correction step's range, kept as one call so that the unrolled
+// epilogue does not carry an inlined division per element.
+static __device__ __noinline__ unsigned long long unscale_div_f32x2(unsigned long long y2, float a) {
+  float y0, y1;
+  unpair_f32(y2, y0, y1);
+  return pair_f32(__fdiv_rn(y0, a), __fdiv_rn(y1, a));
+}
 __device__ __forceinline__ float neg_unscale_f32(float y, const Unscale& u) {
   const float nq0 = __fmul_rn(y, u.nr);
   const float rem = __fmaf_rn(nq0, u.a, y);

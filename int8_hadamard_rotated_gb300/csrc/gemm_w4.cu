@@ -501,11 +501,8 @@ convrot_gemm_w4_kernel(const __grid_constant__ GemmParams p) {
               }
             } else {
               if (UNSCALE) {
-                float a0, a1, a2, a3;
-                unpair_f32(ya, a0, a1);
-                unpair_f32(yb, a2, a3);
-                ya = pair_f32(__fdiv_rn(a0, in_scale), __fdiv_rn(a1, in_scale));
-                yb = pair_f32(__fdiv_rn(a2, in_scale), __fdiv_rn(a3, in_scale));
+                ya = unscale_div_f32x2(ya, in_scale);
+                yb = unscale_div_f32x2(yb, in_scale);
               }
               if (b_ptr) {
                 ya = add_f32x2(ya, bb2);
