@@ -171,17 +171,24 @@ def gemm_traffic(kernel_src_hash):
             for line in f:
                 if line.startswith("traffic_json:"):
                     d = json.loads(line.split(":", 1)[1])
-                    if d.get("gemm_cu_sha256") == kernel_src_hash:
+                    if d.get("gemm_src_sha256") == kernel_src_hash:
                         return d.get("dram_bytes_per_launch")
     except Exception:
         pass
     return None
 
 
+GEMM_SOURCES = ("gemm.cu", "gemm_common.cuh", "common.cuh")
+
+
 def source_hash():
-    p = os.path.join(ROOT, "int8_hadamard_rotated_gb300", "csrc", "gemm.cu")
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()
+    """SHA-256 of the GEMM kernel's sources (gemm.cu, gemm_common.cuh and
+    common.cuh, concatenated in that order)."""
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "int8_hadamard_rotated_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
 
 
 def bench_lib():
