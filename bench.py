@@ -468,6 +468,22 @@ def run_gpu(args, rank, world, local_rank):
         gbs = pack_bytes / (ms * 1e-3) / 1e9
         sweep[str(G)]["back_to_back"] = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
                                          "buffers": nbuf}
+    # the size-matched copy over the same rotating buffers: the back-to-back ceiling
+    bl = bench_lib()
+
+    def copy_all():
+        for i in range(nbuf):
+            st = bl.bench_copy_ceiling(Xr[i].data_ptr(), pw.M, pw.K, 1, Qr[i].data_ptr(), sr[i].data_ptr(), 8, sp)
+            if st != 0:
+                raise RuntimeError(f"bench_copy_ceiling failed: {st}")
+    copy_all()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(passes):
+        copy_all()
+    b.record(stream)
+    torch.cuda.synchronize()
+    cc_b2b = a.elapsed_time(b) / (passes * nbuf) * 1e3  # us
     del Xr, Qr, sr
     # long rows: the MLP pair's repack input, X fp32 [4608, 12288] -> binary16 codes
     ML, KL = 4608, 12288
@@ -493,7 +509,9 @@ def run_gpu(args, rank, world, local_rank):
     ms = float(np.mean([a.elapsed_time(b) for a, b in times]))
     gbs = large_bytes / (ms * 1e-3) / 1e9
     large = {"workload": f"X fp32 [{ML},{KL}] ~N(0,1) seed 4, G=256 -> binary16 codes + s",
-             "bytes": large_bytes, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4)}
+             "bytes": large_bytes, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1), "frac": round(gbs / hbm, 4),
+             "copy_ceiling_us": round(copy_ceiling_us(Xl, 2, flush, stream), 2),
+             "copy_ceiling_note": "size-matched copy (fp32 in, 2 B per element + 4 B per row out), same flush protocol"}
     del Xl, Ql, sl
 
     # ---- the DiT MLP pair on the device (convrot_mlp) ---------------------
@@ -520,7 +538,9 @@ def run_gpu(args, rank, world, local_rank):
         "copy_ceiling": {"what": "size-matched streaming copy (fp32 in, 1 B per element + 4 B per row out), "
                                  "same flush protocol, no pack arithmetic",
                          "us": round(cc_sweep, 2), "GB/s": round(pack_bytes / (cc_sweep * 1e-6) / 1e9, 1),
-                         "frac": round(pack_bytes / (cc_sweep * 1e-6) / 1e9 / hbm, 4)},
+                         "frac": round(pack_bytes / (cc_sweep * 1e-6) / 1e9 / hbm, 4),
+                         "back_to_back_us": round(cc_b2b, 2),
+                         "back_to_back_frac": round(pack_bytes / (cc_b2b * 1e-6) / 1e9 / hbm, 4)},
         "fused_step_pack": {"us": round(pack_us, 2),
                             "bytes": fused_pack_bytes,
                             "bytes_note": "algorithmic: fp32 X in, int8 codes + fp32 row scales out",

@@ -130,21 +130,21 @@ __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t addr) {
 }
 
 // Eight signed 4-bit values (one 32-bit word of the packed row, element 2j in
-// the low nibble of byte j) -> four binary16 pairs in element order. Each
-// pair is built as the bits 0x6400 | (n ^ 8) in both halves, which is the
-// binary16 number 1024 + (v + 8) for the two's-complement nibble n of value
-// v, then 1032 is subtracted: exact, every value and step is an integer
-// below 2^11.
+// the low nibble of byte j) -> four binary16 pairs in element order. Pair k
+// takes byte k into both halves (one byte permute); one LOP3 keeps the low
+// nibble n0 in the low half and the high nibble n1 (at bits 4-7) in the high
+// half and sets the bits 0x6400 | (n0 ^ 8) and 0x6400 | ((n1 ^ 8) << 4): the
+// binary16 numbers 1024 + v0 + 8 and 1024 + 16 (v1 + 8) for the nibbles'
+// two's-complement values v0, v1. One HFMA2, (x0, x1) * (1, 1/16) +
+// (-1032, -72), gives (v0, v1): every product and sum is an integer below
+// 2^11 or that divided by 16 exactly, so the fused operation is exact.
 __device__ __forceinline__ void widen_w4x8(uint32_t w, uint32_t (&h)[4]) {
-  const uint32_t lo = w & 0x0F0F0F0Fu;          // elements 0, 2, 4, 6 (one per byte)
-  const uint32_t hi = (w >> 4) & 0x0F0F0F0Fu;   // elements 1, 3, 5, 7
-  const __half2 bias = __floats2half2_rn(1032.0f, 1032.0f);
+  const __half2 scale = __floats2half2_rn(1.0f, 0.0625f);
+  const __half2 offset = __floats2half2_rn(-1032.0f, -72.0f);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
-    // byte 0 <- lo byte k (element 2k), byte 2 <- hi byte k (element 2k+1)
-    const uint32_t sel = static_cast<uint32_t>(k | (k << 4) | ((4 + k) << 8) | ((4 + k) << 12));
-    const uint32_t t = (__byte_perm(lo, hi, sel) & 0x000F000Fu) ^ 0x64086408u;
-    __half2 v = __hsub2(*reinterpret_cast<const __half2*>(&t), bias);
+    const uint32_t t = (__byte_perm(w, 0u, static_cast<uint32_t>(k | (k << 8))) & 0x00F0000Fu) ^ 0x64806408u;
+    __half2 v = __hfma2(*reinterpret_cast<const __half2*>(&t), scale, offset);
     h[k] = *reinterpret_cast<uint32_t*>(&v);
   }
 }
