@@ -47,6 +47,7 @@
 #include <algorithm>
 #include <atomic>
 #include <chrono>
+#include <type_traits>
 #include <mutex>
 
 namespace convrot {
@@ -425,98 +426,105 @@ convrot_gemm_kernel(const __grid_constant__ GemmParams p) {
             us_fast = unscale_fast_ok(in_scale, lo, hi, sw);
           }
           const unsigned long long m1 = pair_f32(-1.0f, -1.0f);
-          // (unrolled so that the accumulators stay in registers)
+          // The row blocks, once with the correction step (FAST) and once with
+          // the IEEE division, so that the loop that runs is contiguous code
+          // (unrolled so that the accumulators stay in registers).
+          auto row_blocks = [&](auto fast_tag) {
+            constexpr bool FAST = decltype(fast_tag)::value;
 #pragma unroll
-          for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
-            // every block commits one bulk group (empty when nothing is
-            // stored) and the count of blocks per tile is even, so the group
-            // two back is the last store from this buffer: wait until it read it
-            // (split SwiGLU: y is staged in buffer 0, reused every block, and
-            // h in one half of buffer 1 per block, the half two blocks back
-            // being the last one stored)
-            float* sy = reinterpret_cast<float*>(sy_base + (SWIGLU ? 0 : (sub & 1) * Y_BUF_BYTES));
-            if (store_leader) bulk_wait_read<1>();
-            named_bar_sync(1 + half, 4 * 32);
+            for (int sub = 0; sub < COLS_PER_THREAD / Y_ROWS; ++sub) {
+              // every block commits one bulk group (empty when nothing is
+              // stored) and the count of blocks per tile is even, so the group
+              // two back is the last store from this buffer: wait until it read it
+              // (split SwiGLU: y is staged in buffer 0, reused every block, and
+              // h in one half of buffer 1 per block, the half two blocks back
+              // being the last one stored)
+              float* sy = reinterpret_cast<float*>(sy_base + (SWIGLU ? 0 : (sub & 1) * Y_BUF_BYTES));
+              if (store_leader) bulk_wait_read<1>();
+              named_bar_sync(1 + half, 4 * 32);
 #pragma unroll
-            for (int i = 0; i < Y_ROWS; i += 4) {
-              const int idx = sub * Y_ROWS + i;
-              const float4 s4 = *reinterpret_cast<const float4*>(ssx + idx);
-              // float(A) * s_x * s_w (/ input scale) + b, one rounding per
-              // operation, in that order, two rows at once
-              unsigned long long ya = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
-                                                pair_f32(s4.x, s4.y));
-              unsigned long long yb = mul_f32x2(pair_f32(__int_as_float(acc[idx + 2]), __int_as_float(acc[idx + 3])),
-                                                pair_f32(s4.z, s4.w));
-              if (sw_ptr) {
-                ya = mul_f32x2(ya, sw2);
-                yb = mul_f32x2(yb, sw2);
-              }
-              if (UNSCALE && us_fast) {
-                // unscale before the bias: -RN(y / a) by the correction step,
-                // then RN(b - (-q)) or -(-q)
-                ya = neg_unscale_f32x2(ya, us);
-                yb = neg_unscale_f32x2(yb, us);
-                if (b_ptr) {
-                  ya = f32x2_fma(ya, m1, bb2);
-                  yb = f32x2_fma(yb, m1, bb2);
+              for (int i = 0; i < Y_ROWS; i += 4) {
+                const int idx = sub * Y_ROWS + i;
+                const float4 s4 = *reinterpret_cast<const float4*>(ssx + idx);
+                // float(A) * s_x * s_w (/ input scale) + b, one rounding per
+                // operation, in that order, two rows at once
+                unsigned long long ya = mul_f32x2(pair_f32(__int_as_float(acc[idx]), __int_as_float(acc[idx + 1])),
+                                                  pair_f32(s4.x, s4.y));
+                unsigned long long yb = mul_f32x2(pair_f32(__int_as_float(acc[idx + 2]), __int_as_float(acc[idx + 3])),
+                                                  pair_f32(s4.z, s4.w));
+                if (sw_ptr) {
+                  ya = mul_f32x2(ya, sw2);
+                  yb = mul_f32x2(yb, sw2);
+                }
+                if (UNSCALE && FAST) {
+                  // unscale before the bias: -RN(y / a) by the correction step,
+                  // then RN(b - (-q)) or -(-q)
+                  ya = neg_unscale_f32x2(ya, us);
+                  yb = neg_unscale_f32x2(yb, us);
+                  if (b_ptr) {
+                    ya = f32x2_fma(ya, m1, bb2);
+                    yb = f32x2_fma(yb, m1, bb2);
+                  } else {
+                    ya = mul_f32x2(ya, m1);
+                    yb = mul_f32x2(yb, m1);
+                  }
                 } else {
-                  ya = mul_f32x2(ya, m1);
-                  yb = mul_f32x2(yb, m1);
+                  if (UNSCALE && !FAST) {
+                    // unscale before the bias (IEEE division, element by element)
+                    ya = unscale_div_f32x2(ya, in_scale);
+                    yb = unscale_div_f32x2(yb, in_scale);
+                  }
+                  if (b_ptr) {
+                    ya = add_f32x2(ya, bb2);
+                    yb = add_f32x2(yb, bb2);
+                  }
+                }
+                float y0, y1, y2, y3;
+                unpair_f32(ya, y0, y1);
+                unpair_f32(yb, y2, y3);
+                if (ACT == kActGelu) {
+                  gelu_as2(y0, y1);
+                  gelu_as2(y2, y3);
+                }
+                sy[i * CTA_M + col] = y0;
+                sy[(i + 1) * CTA_M + col] = y1;
+                sy[(i + 2) * CTA_M + col] = y2;
+                sy[(i + 3) * CTA_M + col] = y3;
+              }
+              // Split SwiGLU: the product is evaluated by the warps of TMEM
+              // quarters 2 and 3 only (quarter 0 shares its scheduler with the
+              // TMA producer and quarter 1 with the MMA issuer, which pace the
+              // kernel), eight independent rows per thread.
+              const int awork = col - 64;  // 0 .. 63 in quarters 2 and 3
+              if (SWIGLU) {
+                // h = silu(gate) * up for the CTA's 64 features: gate in staged
+                // columns 0-63, up in 64-127
+                named_bar_sync(1 + half, 4 * 32);
+                float* sh = reinterpret_cast<float*>(sy_base + Y_BUF_BYTES) + (sub & 1) * (Y_ROWS * 64);
+                if (awork >= 0) {
+#pragma unroll
+                  for (int i = 0; i < Y_ROWS; ++i)
+                    sh[i * 64 + awork] = silu_mul_fast(sy[i * CTA_M + awork], sy[i * CTA_M + 64 + awork]);
+                }
+                fence_proxy_async_smem();
+                named_bar_sync(1 + half, 4 * 32);
+                if (store_leader) {
+                  const int f0 = c.wt * 128 + static_cast<int>(rank) * 64;
+                  if (f0 < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[0], sh, f0, r0 + sub * Y_ROWS);
+                  bulk_commit();
                 }
               } else {
-                if (UNSCALE) {
-                  // unscale before the bias (IEEE division, element by element)
-                  ya = unscale_div_f32x2(ya, in_scale);
-                  yb = unscale_div_f32x2(yb, in_scale);
-                }
-                if (b_ptr) {
-                  ya = add_f32x2(ya, bb2);
-                  yb = add_f32x2(yb, bb2);
+                fence_proxy_async_smem();
+                named_bar_sync(1 + half, 4 * 32);
+                if (store_leader) {
+                  if (o_base < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
+                  bulk_commit();
                 }
               }
-              float y0, y1, y2, y3;
-              unpair_f32(ya, y0, y1);
-              unpair_f32(yb, y2, y3);
-              if (ACT == kActGelu) {
-                gelu_as2(y0, y1);
-                gelu_as2(y2, y3);
-              }
-              sy[i * CTA_M + col] = y0;
-              sy[(i + 1) * CTA_M + col] = y1;
-              sy[(i + 2) * CTA_M + col] = y2;
-              sy[(i + 3) * CTA_M + col] = y3;
             }
-            // Split SwiGLU: the product is evaluated by the warps of TMEM
-            // quarters 2 and 3 only (quarter 0 shares its scheduler with the
-            // TMA producer and quarter 1 with the MMA issuer, which pace the
-            // kernel), eight independent rows per thread.
-            const int awork = col - 64;  // 0 .. 63 in quarters 2 and 3
-            if (SWIGLU) {
-              // h = silu(gate) * up for the CTA's 64 features: gate in staged
-              // columns 0-63, up in 64-127
-              named_bar_sync(1 + half, 4 * 32);
-              float* sh = reinterpret_cast<float*>(sy_base + Y_BUF_BYTES) + (sub & 1) * (Y_ROWS * 64);
-              if (awork >= 0) {
-#pragma unroll
-                for (int i = 0; i < Y_ROWS; ++i)
-                  sh[i * 64 + awork] = silu_mul_fast(sy[i * CTA_M + awork], sy[i * CTA_M + 64 + awork]);
-              }
-              fence_proxy_async_smem();
-              named_bar_sync(1 + half, 4 * 32);
-              if (store_leader) {
-                const int f0 = c.wt * 128 + static_cast<int>(rank) * 64;
-                if (f0 < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[0], sh, f0, r0 + sub * Y_ROWS);
-                bulk_commit();
-              }
-            } else {
-              fence_proxy_async_smem();
-              named_bar_sync(1 + half, 4 * 32);
-              if (store_leader) {
-                if (o_base < N && r0 + sub * Y_ROWS < p.M) tma_store_2d(&p.tmap_y[c.lin], sy, o_base, r0 + sub * Y_ROWS);
-                bulk_commit();
-              }
-            }
-          }
+          };
+          if (!UNSCALE || us_fast) row_blocks(std::true_type{});
+          else row_blocks(std::false_type{});
         } else {
           Unscale us{};
           bool us_fast = false;
