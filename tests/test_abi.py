@@ -218,3 +218,17 @@ def test_timeout_test_entry_checks(L):
     assert f(A0, A5, 16, 256, wts, 1, A6, sync - 8, 1000, None) == ops.ERR_WORKSPACE
     w4 = (W * 1)(W(None, A2, A3, 64, A4, None, A1))
     assert f(A0, A5, 16, 256, w4, 1, A6, sync, 1000, None) == ops.ERR_ARG        # binary16 weights only
+
+
+def test_unscale_sweep_entry_checks(L):
+    """The unscaling sweep (a test of the GEMM epilogue's division step)
+    checks its arguments before touching the device."""
+    from int8_hadamard_rotated_gb300 import ops
+    f = L.convrot_test_unscale_sweep
+    assert f(None, 4, 0, A5, A6, None) == ops.ERR_ARG           # no divisors
+    assert f(A0, 0, 0, A5, A6, None) == ops.ERR_ARG             # empty
+    assert f(A0, 65536, 0, A5, A6, None) == ops.ERR_ARG         # more than a grid's y extent
+    assert f(A0, 4, -99, A5, A6, None) == ops.ERR_ARG           # y below the step's range
+    assert f(A0, 4, 98, A5, A6, None) == ops.ERR_ARG            # y above it
+    assert f(A0, 4, 0, None, A6, None) == ops.ERR_ARG           # no counter
+    assert f(A0 + 4, 4, 0, A5, A6, None) == ops.ERR_ALIGN       # divisors not 16-byte aligned
