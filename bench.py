@@ -680,50 +680,32 @@ def mlp_leg(dev, flush, peak_tf, hbm, peak_kind, with_cpu=True, reps=10):
         Yh.copy_(Ym, non_blocking=True)
     t_seq = timed(e2e_call, n=5)
 
-    # the same, pipelined over row chunks: chunk c's copy in, its convrot_mlp call and its copy
-    # out run on three streams, ordered by events, so that transfers overlap the other chunks'
-    # compute (rows are independent; chunks of >= 1152 rows keep the down GEMM's tiles on most SMs)
+    # the same through convrot_mlp_host: row chunks whose copies in and out run on two copy
+    # streams, overlapping the other chunks' compute (the library default is 1536 rows)
     copy_in, copy_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    Yh2 = torch.empty_like(Yh).pin_memory()
 
-    def e2e_chunked(nch):
-        rows = M // nch
-        wsc = torch.empty((ops.convrot_mlp_workspace_size(rows, K, N_up),), dtype=torch.uint8, device=dev)
-
-        def call():
-            copy_in.wait_stream(stream)
-            for c in range(nch):
-                r0, r1 = c * rows, (c + 1) * rows
-                with torch.cuda.stream(copy_in):
-                    Xd[r0:r1].copy_(Xh[r0:r1], non_blocking=True)
-                e_in = torch.cuda.Event()
-                e_in.record(copy_in)
-                stream.wait_event(e_in)
-                ops.convrot_mlp(Xd[r0:r1], G, mlp_w[0], ops.ACT_GELU, G, mlp_w[1], Y=Ym[r0:r1], workspace=wsc,
-                                stream=stream)
-                e_done = torch.cuda.Event()
-                e_done.record(stream)
-                copy_out.wait_event(e_done)
-                with torch.cuda.stream(copy_out):
-                    Yh[r0:r1].copy_(Ym[r0:r1], non_blocking=True)
-            stream.wait_stream(copy_out)
-        return call
-    chunked = {n: timed(e2e_chunked(n), n=5) for n in (2, 3, 4) if M % n == 0}
-    best_n = min(chunked, key=chunked.get)
-    t_e2e = chunked[best_n]
+    def host_call(rows):
+        wsh = torch.empty((ops.convrot_mlp_host_workspace_size(M, K, ops.F32, N_up, N_down, rows),),
+                          dtype=torch.uint8, device=dev)
+        return lambda: ops.convrot_mlp_host(Xh, G, mlp_w[0], ops.ACT_GELU, G, mlp_w[1], Y=Yh2, chunk_rows=rows,
+                                            workspace=wsh, stream=stream, copy_in_stream=copy_in,
+                                            copy_out_stream=copy_out)
+    by_rows = {rows: timed(host_call(rows), n=5) for rows in (1152, 1536, 2304)}
+    t_e2e = timed(host_call(0), n=5)
     e2e = {"value": round((ops_up + ops_down) / (t_e2e * 1e-6) / 1e12, 2), "unit": "TOPS", "us": round(t_e2e, 2),
            "h2d_bytes_per_step": int(Xh.numel() * 4), "d2h_bytes_per_step": int(Yh.numel() * 4),
-           "api": f"convrot_mlp on {best_n} row chunks of {M // best_n}, pinned host X in and Y out on copy "
-                  f"streams overlapped with the other chunks' compute",
-           "us_by_chunks": {str(n): round(t, 2) for n, t in chunked.items()},
+           "api": "convrot_mlp_host (one call; pinned host X and Y, row chunks of 1536 whose copies overlap "
+                  "the other chunks' compute)",
+           "us_by_chunk_rows": {str(r): round(t, 2) for r, t in by_rows.items()},
            "sequential": {"us": round(t_seq, 2), "TOPS": round((ops_up + ops_down) / (t_seq * 1e-6) / 1e12, 2),
                           "api": "copy X host->device, one convrot_mlp call, copy Y device->host"}}
     # the pipelined result equals the one-call result
-    e2e_chunked(best_n)()
-    torch.cuda.synchronize()
-    Y_ref = Ym.cpu()
+    host_call(0)()
     e2e_call()
     torch.cuda.synchronize()
-    e2e["parity_max_abs_diff_vs_one_call"] = float((Y_ref - Yh).abs().max().item())
+    e2e["parity_max_abs_diff_vs_one_call"] = float((Yh2 - Yh).abs().max().item())
+    del Yh2
     del Xh, Yh, Xd
 
     # split SwiGLU: gate and up [12288, 3072] sharing the pack, h = silu(gate) * up

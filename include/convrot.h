@@ -460,6 +460,37 @@ int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int G_up,
                 void* stream);
 
 /*
+ * convrot_mlp_host_workspace_size -- device bytes convrot_mlp_host needs: two
+ * sets of chunk buffers (input rows, output rows) and one convrot_mlp
+ * workspace for a chunk. chunk_rows = 0 picks the default (1536 rows).
+ * Returns 0 for invalid arguments.
+ */
+size_t convrot_mlp_host_workspace_size(int64_t M, int64_t K, int x_dtype, int64_t N_up,
+                                       int64_t N_down, int64_t chunk_rows);
+
+/*
+ * convrot_mlp_host -- convrot_mlp with X and Y in HOST memory (weights,
+ * scales and biases in device memory). The rows are independent, so they are
+ * processed in chunks of chunk_rows: each chunk is copied in on
+ * copy_in_stream, run through convrot_mlp on `stream`, and its rows of Y
+ * copied out on copy_out_stream, so transfers overlap the other chunks'
+ * compute. Results equal convrot_mlp's bit for bit. Host arrays should be
+ * pinned for the transfers to overlap.
+ *   X_host     [M,K] fp32/fp16 host array;  Y_host [M,N_down] fp32 host array.
+ *   up, activation, down, G_up, G_down: as convrot_mlp; the descriptors' Y
+ *              fields are ignored (H stays in the workspace, Y goes to Y_host).
+ *   chunk_rows rows per chunk (0 = 1536; chunks much smaller than that leave
+ *              the down GEMM's tiles on few SMs).
+ *   workspace  device scratch, >= convrot_mlp_host_workspace_size(...).
+ *   stream, copy_in_stream, copy_out_stream: as convrot_linear_host.
+ * Errors: as convrot_mlp.
+ */
+int convrot_mlp_host(const void* X_host, int x_dtype, int64_t M, int64_t K, int G_up,
+                     const convrot_weight* up, int activation, int G_down, const convrot_weight* down,
+                     float* Y_host, int64_t chunk_rows, void* workspace, size_t workspace_bytes,
+                     void* stream, void* copy_in_stream, void* copy_out_stream);
+
+/*
  * convrot_linear_swiglu -- split SwiGLU of two linears that share an input
  * ("ggml operator extensions", sd.cpp integration: two INT8 GEMMs sharing a
  * quantized input fuse with split SwiGLU, a paired-column iterator reads the
@@ -467,7 +498,9 @@ int convrot_mlp(const void* X, int x_dtype, int64_t M, int64_t K, int G_up,
  * activated output): X is packed once, and one GEMM computes
  *   g = float(Q_x Q_gate^T) * s_x * s_gate + b_gate,
  *   u = float(Q_x Q_up^T) * s_x * s_up + b_up,
- *   h = silu(g) * u = (g / (1 + exp(-g))) * u   (fp32, expf, IEEE division),
+ *   h = silu(g) * u = (g / (1 + exp(-g))) * u   (fp32: the hardware base-2
+ *       exponential and a correctly rounded reciprocal, relative error of a
+ *       few 1e-7),
  * writing h only.
  *   gate_up  host array of two descriptors: the gate linear, then the up
  *            linear; binary16 weights (q16), the same N (N % 4 == 0); h is

@@ -102,6 +102,9 @@ SIGNATURES = {
     "convrot_linear_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I64, _VP, _SZ,
                                  _VP, _VP, _VP]),
     "convrot_mlp_workspace_size": (_SZ, [_I64, _I64, _I64]),
+    "convrot_mlp_host_workspace_size": (_SZ, [_I64, _I64, _I, _I64, _I64, _I64]),
+    "convrot_mlp_host": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I,
+                              ctypes.POINTER(convrot_weight), _VP, _I64, _VP, _SZ, _VP, _VP, _VP]),
     "convrot_mlp": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _I,
                          ctypes.POINTER(convrot_weight), _VP, _SZ, _VP]),
     "convrot_linear_noalloc": (_I, [_VP, _I, _I64, _I64, _I, ctypes.POINTER(convrot_weight), _I, _VP]),
@@ -522,6 +525,41 @@ def convrot_mlp(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: 
     ws = _workspace(convrot_mlp_workspace_size(M, K, N_up), X.device, workspace)
     _check(lib().convrot_mlp(_ptr(X), xd, M, K, G_up, wu, activation, G_down, wd, _ptr(ws), ws.numel(),
                              _stream(stream)), "convrot_mlp")
+    return Y
+
+
+def convrot_mlp_host_workspace_size(M: int, K: int, x_dtype: int, N_up: int, N_down: int,
+                                    chunk_rows: int = 0) -> int:
+    return int(lib().convrot_mlp_host_workspace_size(M, K, x_dtype, N_up, N_down, chunk_rows))
+
+
+def convrot_mlp_host(X: torch.Tensor, G_up: int, up: Tuple, activation: int, G_down: int, down: Tuple,
+                     Y: Optional[torch.Tensor] = None, chunk_rows: int = 0, workspace=None, stream=None,
+                     copy_in_stream=None, copy_out_stream=None) -> torch.Tensor:
+    """convrot_mlp on host arrays: X [M,K] and Y [M,N_down] live in (pinned)
+    host memory, the weights on the device; row chunks are copied in, run
+    and copied out on three streams so that transfers overlap compute. `up`
+    and `down` as in convrot_mlp."""
+    xd = _xdtype(X)
+    if X.is_cuda or not X.is_contiguous():
+        raise ValueError("X must be a contiguous host tensor")
+    M, K = X.shape
+    ups = list(up) if activation == ACT_SWIGLU else [up]
+    dq, ds, db, dk = down
+    N_up, N_down = ups[0][0].shape[0], dq.shape[0]
+    dev = dq.device
+    if Y is None:
+        Y = torch.empty((M, N_down), dtype=torch.float32, pin_memory=True)
+    if Y.is_cuda or Y.dtype != torch.float32 or not Y.is_contiguous():
+        raise ValueError("Y must be a contiguous float32 host tensor")
+    wu = make_weights([u[0] for u in ups], [u[1] for u in ups], [u[2] for u in ups], [None] * len(ups),
+                      [u[3] for u in ups])
+    wd = make_weights([dq], [ds], [db], [None], [dk])
+    ws = _workspace(convrot_mlp_host_workspace_size(M, K, xd, N_up, N_down, chunk_rows), dev, workspace)
+    _check(lib().convrot_mlp_host(X.data_ptr(), xd, M, K, G_up, wu, activation, G_down, wd, Y.data_ptr(),
+                                  chunk_rows, _ptr(ws), ws.numel(), _stream(stream),
+                                  _stream(copy_in_stream) if copy_in_stream else None,
+                                  _stream(copy_out_stream) if copy_out_stream else None), "convrot_mlp_host")
     return Y
 
 

@@ -232,3 +232,25 @@ def test_unscale_sweep_entry_checks(L):
     assert f(A0, 4, 98, A5, A6, None) == ops.ERR_ARG            # y above it
     assert f(A0, 4, 0, None, A6, None) == ops.ERR_ARG           # no counter
     assert f(A0 + 4, 4, 0, A5, A6, None) == ops.ERR_ALIGN       # divisors not 16-byte aligned
+
+
+def test_mlp_host_argument_checks(L):
+    """convrot_mlp_host checks its arguments before touching the device."""
+    from int8_hadamard_rotated_gb300 import ops
+    W = ops.convrot_weight
+    up = (W * 1)(W(A1, A2, A3, 256, None, None))
+    down = (W * 1)(W(A4, A2, A3, 64, None, None))
+    f = L.convrot_mlp_host
+    need = L.convrot_mlp_host_workspace_size(16, 64, ops.F32, 256, 64, 0)
+    assert need > 0
+    assert L.convrot_mlp_host_workspace_size(16, 64, 7, 256, 64, 0) == 0          # bad dtype
+    assert f(None, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, 0, A6, need, None, None, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, None, 0, A6, need, None, None, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 64, 64, up, 9, 64, down, A5, 0, A6, need, None, None, None) == ops.ERR_ARG
+    assert f(A0, 7, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, 0, A6, need, None, None, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, -1, A6, need, None, None, None) == ops.ERR_ARG
+    assert f(A0, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, 0, None, 0, None, None, None) == ops.ERR_WORKSPACE
+    assert f(A0, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, 0, A6, need - 256, None, None,
+             None) == ops.ERR_WORKSPACE
+    assert f(A0, ops.F32, 16, 64, 64, up, ops.ACT_GELU, 64, down, A5, 0, A6 + 8, need, None, None,
+             None) == ops.ERR_ALIGN

@@ -151,3 +151,34 @@ def test_mlp_without_activation_is_two_linears(ops):
     (Y1,) = ops.convrot_linear(dev(X), G1, [h1], [s1], [dev(b1)])
     (Y2,) = ops.convrot_linear(Y1, G2, [h2], [s2], [dev(b2)])
     np.testing.assert_array_equal(Y, host(Y2))
+
+
+@pytest.mark.parametrize("act,M,chunk_rows", [("gelu", 1000, 384), ("swiglu", 700, 256), ("gelu", 4608, 0)])
+def test_mlp_host_equals_device_call(ops, act, M, chunk_rows):
+    """convrot_mlp_host (host X and Y, row chunks whose copies overlap the
+    other chunks' compute; a ragged last chunk in the first two cases, the
+    default chunks on the DiT MLP in the last) gives convrot_mlp's output bit
+    for bit: the rows are independent and every step is exact or rounds the
+    same values in the same order."""
+    K, G = 3072, 256
+    N_up = 12288 if M == 4608 else 4096
+    rng = workloads.rng_for(M + N_up)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0)
+    Wu, Wd = workloads.weights(rng, N_up, K), workloads.weights(rng, K, N_up)
+    bu, bd = workloads.biases(rng, N_up), workloads.biases(rng, K)
+    u, d = prepared(ops, Wu, G), prepared(ops, Wd, G)
+    up = (u[2], u[1], dev(bu), u[3])
+    if act == "swiglu":
+        Wg, bg = workloads.weights(rng, N_up, K), workloads.biases(rng, N_up)
+        g = prepared(ops, Wg, G)
+        up = ((g[2], g[1], dev(bg), g[3]), up)
+    a = ops.ACT_SWIGLU if act == "swiglu" else ops.ACT_GELU
+    down = (d[2], d[1], dev(bd), d[3])
+    Y_dev = host(ops.convrot_mlp(dev(X), G, up, a, G, down))
+    Xh = torch.from_numpy(X).pin_memory()
+    copy_in, copy_out = torch.cuda.Stream(), torch.cuda.Stream()
+    Y_host = ops.convrot_mlp_host(Xh, G, up, a, G, down, chunk_rows=chunk_rows, copy_in_stream=copy_in,
+                                  copy_out_stream=copy_out)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(Y_host.numpy(), Y_dev)
+    assert ops.convrot_device_status() == ops.OK
