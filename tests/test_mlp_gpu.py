@@ -153,8 +153,9 @@ def test_mlp_without_activation_is_two_linears(ops):
     np.testing.assert_array_equal(Y, host(Y2))
 
 
-@pytest.mark.parametrize("act,M,chunk_rows", [("gelu", 1000, 384), ("swiglu", 700, 256), ("gelu", 4608, 0)])
-def test_mlp_host_equals_device_call(ops, act, M, chunk_rows):
+@pytest.mark.parametrize("act,M,chunk_rows,x_dtype", [("gelu", 1000, 384, "f32"), ("swiglu", 700, 256, "f32"),
+                                                       ("gelu", 4608, 0, "f32"), ("gelu", 520, 256, "f16")])
+def test_mlp_host_equals_device_call(ops, act, M, chunk_rows, x_dtype):
     """convrot_mlp_host (host X and Y, row chunks whose copies overlap the
     other chunks' compute; a ragged last chunk in the first two cases, the
     default chunks on the DiT MLP in the last) gives convrot_mlp's output bit
@@ -163,7 +164,7 @@ def test_mlp_host_equals_device_call(ops, act, M, chunk_rows):
     K, G = 3072, 256
     N_up = 12288 if M == 4608 else 4096
     rng = workloads.rng_for(M + N_up)
-    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0)
+    X = workloads.activations(rng, M, K, outlier_frac=0.01, outlier_mult=40.0, dtype=x_dtype)
     Wu, Wd = workloads.weights(rng, N_up, K), workloads.weights(rng, K, N_up)
     bu, bd = workloads.biases(rng, N_up), workloads.biases(rng, K)
     u, d = prepared(ops, Wu, G), prepared(ops, Wd, G)
